@@ -1,0 +1,177 @@
+"""CPU parity oracle (test infrastructure).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline /
+reference leg may import this package. The product path never does.
+
+The arithmetic lives in ``oracle.cpp`` (plain single-threaded C++17, built
+with ``-ffp-contract=off``); this module only compiles it and marshals numpy
+arrays through ctypes.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle.so")
+# A prebuilt oracle library to load instead (the mutation tests point this at a
+# copy of the oracle with a planted mistake).
+_LIB_OVERRIDE = os.environ.get("USC_ORACLE_LIB")
+_lib = None
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+
+
+def compile_library(src: str, out: str) -> str:
+    """Compile one oracle source file into a shared library."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+           "-shared", "-o", tmp, src]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.cpp into liboracle.so (next to it)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        compile_library(_SRC, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if _LIB_OVERRIDE:
+            lib = ctypes.CDLL(_LIB_OVERRIDE)
+        else:
+            build()
+            lib = ctypes.CDLL(_LIB)
+        lib.oracle_batching.restype = _I32
+        lib.oracle_batching.argtypes = [
+            _P, _I32, _P, _I64, _P, _I64, _P, _P, _P,
+            _I64, _I64, _I64, _I64, _I64, _I64, _I64,
+            _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+        lib.oracle_unpermute.restype = _I32
+        lib.oracle_unpermute.argtypes = [
+            _P, _P, _P, _P, _I64, _I64, _I32, _I64, _I32, _I64, _I64, _I32,
+            _P, _P, _P, _P]
+        for name in ("oracle_half_to_float", "oracle_float_to_half", "oracle_bf16_to_float",
+                     "oracle_float_to_bf16"):
+            getattr(lib, name).restype = None
+            getattr(lib, name).argtypes = [_P, _P, _I64]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle arrays must be contiguous"
+    return a.ctypes.data
+
+
+# -- conversions (exported for the conversion pins) -------------------------
+
+def half_to_float(bits: np.ndarray) -> np.ndarray:
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, dtype=np.float32)
+    _load().oracle_half_to_float(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def float_to_half(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().oracle_float_to_half(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def bf16_to_float(bits: np.ndarray) -> np.ndarray:
+    bits = np.ascontiguousarray(bits, dtype=np.uint16)
+    out = np.empty(bits.shape, dtype=np.float32)
+    _load().oracle_bf16_to_float(_ptr(bits), _ptr(out), bits.size)
+    return out
+
+
+def float_to_bf16(x: np.ndarray) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().oracle_float_to_bf16(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+# -- the two operations -------------------------------------------------------
+
+ELEM_BYTES = {0: 2, 1: 2, 2: 1, 3: 4}
+
+
+def batching(inp: dict, *, with_gather_idx: bool = False) -> dict:
+    """Run the batching oracle on a ``workloads.make_batching`` dict.
+    Returns y (uint8 [Y, H*s]), groupList, sessionIds, microBatchIds, tokenIds,
+    expertOffsets, dynamicScale (None unless int8), actualTokenNum (int),
+    sortedIndices (slot -> output row or -1) and optionally gather_idx."""
+    Y, H, dt = inp["Y"], inp["H"], inp["tokenDtype"]
+    E = inp["expertNum"]
+    row_bytes = H * ELEM_BYTES[dt]
+    y = np.zeros((Y, row_bytes), dtype=np.uint8)
+    gl = np.empty((E, 2), dtype=np.int64)
+    sess = np.empty(Y, dtype=np.int32)
+    micro = np.empty(Y, dtype=np.int32)
+    tok = np.empty(Y, dtype=np.int32)
+    eoff = np.empty(Y, dtype=np.int32)
+    dyn = np.zeros(Y, dtype=np.float32) if dt == 2 else None
+    atn = np.zeros(1, dtype=np.int64)
+    sidx = np.empty(Y, dtype=np.int32)
+    gidx = np.empty(Y, dtype=np.int32) if with_gather_idx else None
+    scales = inp.get("scales")
+    scale_stride = 4 if scales is not None else 0
+    td = np.ascontiguousarray(inp["token_data"])
+    rc = _load().oracle_batching(
+        _ptr(np.ascontiguousarray(inp["expert_ids"], dtype=np.int32)), inp["layer_id"],
+        _ptr(td), inp["row_stride"], _ptr(scales), scale_stride,
+        _ptr(inp["session_in"]), _ptr(inp["micro_in"]), _ptr(inp.get("token_in")),
+        E, inp["A"], inp["BS"], inp["K1"], H, dt, inp["layerNum"],
+        _ptr(y), _ptr(gl), _ptr(sess), _ptr(micro), _ptr(tok), _ptr(eoff), _ptr(dyn),
+        _ptr(atn), _ptr(sidx), _ptr(gidx))
+    if rc != 0:
+        raise ValueError(f"oracle_batching rejected its arguments (code {rc})")
+    out = dict(y=y, groupList=gl, sessionIds=sess, microBatchIds=micro, tokenIds=tok,
+               expertOffsets=eoff, dynamicScale=dyn, actualTokenNum=int(atn[0]),
+               sortedIndices=sidx)
+    if with_gather_idx:
+        out["gather_idx"] = gidx
+    return out
+
+
+def unpermute(inp: dict) -> dict:
+    """Run the unpermute oracle on a ``workloads.make_unpermute_*`` dict (keys
+    permuted, sortedIndices, routingMap, probs, permutedRows, H, tokenDtype, n,
+    probsDtype, T, Eu, padded). Returns unpermuted (storage dtype [T, H]),
+    outIndex, permuteTokenId, permuteProbs (None without probs)."""
+    T, H, dt, n = inp["T"], inp["H"], inp["tokenDtype"], inp["n"]
+    probs = inp.get("probs")
+    pdt = inp["probsDtype"]
+    store = np.float32 if dt == 3 else np.uint16
+    out = np.zeros((T, H), dtype=store)
+    oidx = np.empty(n, dtype=np.int32)
+    ptid = np.empty(n, dtype=np.int32)
+    pp = None
+    if probs is not None:
+        pp = np.zeros(n, dtype=np.float32 if pdt == 3 else np.uint16)
+    rmap = inp.get("routingMap") if probs is not None else None
+    rc = _load().oracle_unpermute(
+        _ptr(np.ascontiguousarray(inp["permuted"])), _ptr(np.ascontiguousarray(inp["sortedIndices"])),
+        _ptr(None if rmap is None else np.ascontiguousarray(rmap)),
+        _ptr(None if probs is None else np.ascontiguousarray(probs)),
+        inp["permutedRows"], H, dt, n, pdt, T, inp.get("Eu", 0), int(inp["padded"]),
+        _ptr(out), _ptr(oidx), _ptr(ptid), _ptr(pp))
+    if rc != 0:
+        raise ValueError(f"oracle_unpermute rejected its arguments (code {rc})")
+    return dict(unpermuted=out, outIndex=oidx, permuteTokenId=ptid, permuteProbs=pp)

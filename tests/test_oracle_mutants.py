@@ -1,0 +1,98 @@
+"""The pins catch plausible mistakes.
+
+Each case plants one mistake in a temporary copy of the oracle source (never
+in the committed oracle), builds it on the CPU, and runs the pin suite against
+that library. The suite must fail for every mutant.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+import oracle
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+SRC = os.path.join(ROOT, "oracle", "oracle.cpp")
+
+# (name, text in oracle.cpp, replacement)
+MUTANTS = [
+    ("unstable_sort",
+     "std::stable_sort(gather_idx.begin(), gather_idx.end(),",
+     "std::sort(gather_idx.begin(), gather_idx.end(),"),
+    ("masked_keys_first",
+     "? (int64_t)layer_id * El + id : E;",
+     "? (int64_t)layer_id * El + id : -1;"),
+    ("layer_offset_dropped",
+     "? (int64_t)layer_id * El + id : E;",
+     "? id : E;"),
+    ("offset_off_by_one",
+     "expert_offsets[i] = (int32_t)(i - group_start);",
+     "expert_offsets[i] = (int32_t)(i - group_start + 1);"),
+    ("gather_wrong_row",
+     "token_data + (size_t)(g * row_stride),",
+     "token_data + (size_t)(i * row_stride),"),
+    ("scale_wrong_offset",
+     ": token_data + (size_t)(g * row_stride + H);",
+     ": token_data + (size_t)(g * row_stride + H - 4);"),
+    ("token_id_not_looked_up",
+     "token_out[i] = token_in ? token_in[g] : (int32_t)g;",
+     "token_out[i] = token_in ? token_in[i] : (int32_t)g;"),
+    ("tail_ids_not_minus_one",
+     "token_out[i] = -1;",
+     "token_out[i] = 0;"),
+    ("masked_select_not_transposed",
+     "if (routingMap[t * Eu + e] != 0) {\n                    if (pos < n) copy_elem(permuteProbs, pos, probs, t * Eu + e, probsDtype);",
+     "if (routingMap[e * T + t] != 0) {\n                    if (pos < n) copy_elem(permuteProbs, pos, probs, e * T + t, probsDtype);"),
+    ("padded_prob_index_mod",
+     "copy_elem(permuteProbs, i, probs, v * Eu + i / capacity, probsDtype);",
+     "copy_elem(permuteProbs, i, probs, v * Eu + i % capacity, probsDtype);"),
+    ("weight_dropped",
+     "if (has_probs) term = x * p;\n                acc[(size_t)(t * H + h)] = acc[(size_t)(t * H + h)] + term;\n            }\n        }\n    } else {",
+     "term = x;\n                acc[(size_t)(t * H + h)] = acc[(size_t)(t * H + h)] + term;\n            }\n        }\n    } else {"),
+    ("token_index_mod",
+     "const int64_t t = i / topK;",
+     "const int64_t t = i % T;"),
+    ("zero_prob_not_skipped",
+     "p = weight[i];\n                if (p == 0.0f) continue;",
+     "p = weight[i];"),
+    ("invalid_not_skipped",
+     "if (v < 0 || v >= permutedRows) continue;",
+     "if (v < 0) continue;"),
+    ("padded_invalid_first",
+     "sort_key[i] = (v >= 0 && v < T) ? v : T;  // invalid last",
+     "sort_key[i] = (v >= 0 && v < T) ? v : -1;"),
+    ("not_padded_invalid_last",
+     "sort_key[i] = (v >= 0 && v < permutedRows) ? v : -1;  // invalid first",
+     "sort_key[i] = (v >= 0 && v < permutedRows) ? v : permutedRows;"),
+    ("permute_token_id_mod",
+     "permuteTokenId[i] = padded ? sortedIndices[order[i]] : (int32_t)(order[i] / topK);",
+     "permuteTokenId[i] = padded ? sortedIndices[order[i]] : (int32_t)(order[i] % topK);"),
+    ("bf16_truncates",
+     "if (rest > 0x8000u || (rest == 0x8000u && (keep & 1u))) keep += 1;",
+     ""),
+    ("half_ties_away",
+     "if (rest > 0x1000u || (rest == 0x1000u && (keep & 1u))) r += 1;",
+     "if (rest >= 0x1000u) r += 1;"),
+    ("accumulate_descending",
+     "for (int64_t i = 0; i < n; ++i) {\n            const int64_t v = sortedIndices[i];\n            if (v < 0 || v >= permutedRows) continue;",
+     "for (int64_t i = n - 1; i >= 0; --i) {\n            const int64_t v = sortedIndices[i];\n            if (v < 0 || v >= permutedRows) continue;"),
+    ("double_weighting",
+     "if (has_probs) term = x * p;\n                acc[(size_t)(t * H + h)] = acc[(size_t)(t * H + h)] + term;\n            }\n        }\n    } else {",
+     "if (has_probs) term = (x * p) * p;\n                acc[(size_t)(t * H + h)] = acc[(size_t)(t * H + h)] + term;\n            }\n        }\n    } else {"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(name, old, new, tmp_path):
+    src = open(SRC).read()
+    assert src.count(old) == 1, f"mutant {name}: anchor text not found exactly once"
+    mutant_src = tmp_path / "oracle_mutant.cpp"
+    mutant_src.write_text(src.replace(old, new))
+    lib = oracle.compile_library(str(mutant_src), str(tmp_path / "liboracle_mutant.so"))
+    env = dict(os.environ, USC_ORACLE_LIB=lib)
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(HERE, "test_oracle_pins.py")],
+                       cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"

@@ -1,0 +1,259 @@
+"""Seeded synthetic inputs for the MoE expert-grouped token reorder.
+
+This module only draws inputs. It holds none of the arithmetic of the two
+operations (no sort of slots by expert, no gather, no weighted reduction), so
+the CPU oracle and the CUDA path can both be fed from it without sharing any
+of the method's code. Every array is a numpy array in host memory; the same
+bytes go to both sides.
+
+Workload recipes follow the shapes and distributions of the pages' workloads:
+
+* batching ("aclnnFfnWorkerBatching", 参数说明 and 调用示例): Y = A*BS*(topK+1)
+  slots, each with a local expert id (masked slots carry INT32_MAX), a hidden
+  row (fp16/bf16 ~ N(0,1), or int8 with a trailing fp32 dynamic scale), and
+  session / micro-batch / token ids;
+* unpermute ("MoeTokenUnpermuteWithRoutingMap 算子全解析", 参数说明 and
+  补充说明): permutedTokens, sortedIndices, a (tokens, experts) routing map
+  and probs, in the padded (expert capacity) or the slot layout.
+
+Random streams are numpy PCG64 generators seeded with [seed, tag, block], so
+a value does not depend on how many threads drew it.
+"""
+from __future__ import annotations
+
+import concurrent.futures as _fut
+import os
+
+import numpy as np
+import torch
+
+INT32_MAX = 2**31 - 1
+
+DT_F16, DT_BF16, DT_INT8, DT_F32 = 0, 1, 2, 3
+DTYPE_NAMES = {DT_F16: "f16", DT_BF16: "bf16", DT_INT8: "int8", DT_F32: "f32"}
+ELEM_BYTES = {DT_F16: 2, DT_BF16: 2, DT_INT8: 1, DT_F32: 4}
+
+_ROW_BLOCK = 2048
+_TAG_HIDDEN, _TAG_IDS, _TAG_MASK, _TAG_SESS, _TAG_SCALE, _TAG_ROUTE, _TAG_PROBS = range(7)
+
+
+def _rng(seed: int, *tags: int) -> np.random.Generator:
+    return np.random.default_rng([int(seed), *[int(t) for t in tags]])
+
+
+def _threads() -> int:
+    return max(1, min(32, os.cpu_count() or 1))
+
+
+def _to_storage(x32: np.ndarray, dtype: int) -> np.ndarray:
+    """fp32 samples -> storage of the given float dtype (uint16 bits for 16-bit
+    types, float32 itself for fp32). Uses torch's own round-to-nearest-even
+    conversion."""
+    if dtype == DT_F32:
+        return np.ascontiguousarray(x32, dtype=np.float32)
+    tdt = torch.float16 if dtype == DT_F16 else torch.bfloat16
+    t = torch.from_numpy(np.ascontiguousarray(x32)).to(tdt)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def normal_rows(rows: int, H: int, dtype: int, seed: int, tag: int = _TAG_HIDDEN) -> np.ndarray:
+    """rows x H values ~ N(0,1) in the given float dtype (uint16 bits or float32).
+    Drawn block by block in parallel; block b uses stream [seed, tag, b]."""
+    out = np.empty((rows, H), dtype=np.float32 if dtype == DT_F32 else np.uint16)
+    nblk = (rows + _ROW_BLOCK - 1) // _ROW_BLOCK
+
+    def fill(b: int) -> None:
+        r0 = b * _ROW_BLOCK
+        r1 = min(rows, r0 + _ROW_BLOCK)
+        x = _rng(seed, tag, b).standard_normal((r1 - r0, H), dtype=np.float32)
+        out[r0:r1] = _to_storage(x, dtype)
+
+    if nblk <= 1:
+        for b in range(nblk):
+            fill(b)
+    else:
+        with _fut.ThreadPoolExecutor(_threads()) as ex:
+            list(ex.map(fill, range(nblk)))
+    return out
+
+
+def zipf_ids(n: int, num: int, s: float, rng: np.random.Generator) -> np.ndarray:
+    """n draws of a Zipf(s) law over ranks 1..num, returned as rank-1 (id 0 is
+    the most frequent). Inverse-CDF sampling."""
+    w = np.arange(1, num + 1, dtype=np.float64) ** (-float(s))
+    cdf = np.cumsum(w) / w.sum()
+    u = rng.random(n)
+    return np.minimum(np.searchsorted(cdf, u, side="right"), num - 1).astype(np.int32)
+
+
+# ---------------------------------------------------------------------------
+# Batching inputs
+# ---------------------------------------------------------------------------
+
+def make_batching(*, A: int, BS: int, K1: int, E: int, H: int, dtype: int, layerNum: int = 1,
+                  layer_id: int = 0, ids: str = "uniform", zipf_s: float = 1.1, mask: float = 0.1,
+                  session: int = 2, micro: int = 4, token_ids: bool = True, seed: int = 0,
+                  separate_scales: bool = False) -> dict:
+    """Flat-tensor inputs of one batching call.
+
+    expert_ids: local ids in [0, E/layerNum); masked slots carry INT32_MAX.
+    token_data: uint8 [Y, row_stride]; fp16/bf16 rows hold H values, int8 rows
+    hold H int8 values followed by a little-endian fp32 dynamic scale
+    (row_stride = H + 4) unless separate_scales, in which case the scales are a
+    separate float32 [Y] array and row_stride = H.
+    """
+    Y = A * BS * K1
+    L = max(layerNum, 1)
+    El = E // L
+    rng_ids = _rng(seed, _TAG_IDS)
+    if ids == "uniform":
+        expert = rng_ids.integers(0, El, size=Y, dtype=np.int64).astype(np.int32)
+    elif ids == "zipf":
+        expert = zipf_ids(Y, El, zipf_s, rng_ids)
+    elif ids == "mod":
+        expert = (np.arange(Y) % El).astype(np.int32)
+    else:
+        raise ValueError(ids)
+    if mask > 0:
+        m = _rng(seed, _TAG_MASK).random(Y) < mask
+        expert = np.where(m, np.int32(INT32_MAX), expert).astype(np.int32)
+
+    scales = None
+    if dtype == DT_INT8:
+        rng_h = _rng(seed, _TAG_HIDDEN)
+        data = rng_h.integers(-127, 128, size=(Y, H), dtype=np.int16).astype(np.int8)
+        sc = _rng(seed, _TAG_SCALE).lognormal(mean=-4.0, sigma=0.5, size=Y).astype(np.float32)
+        if separate_scales:
+            token_data = data.view(np.uint8).copy()
+            scales = sc
+            row_stride = H
+        else:
+            token_data = np.empty((Y, H + 4), dtype=np.uint8)
+            token_data[:, :H] = data.view(np.uint8)
+            token_data[:, H:] = sc.view(np.uint8).reshape(Y, 4)
+            row_stride = H + 4
+    else:
+        token_data = normal_rows(Y, H, dtype, seed).view(np.uint8).reshape(Y, H * ELEM_BYTES[dtype])
+        row_stride = H * ELEM_BYTES[dtype]
+
+    rng_s = _rng(seed, _TAG_SESS)
+    session_in = rng_s.integers(0, session, size=Y, dtype=np.int64).astype(np.int32)
+    micro_in = rng_s.integers(0, micro, size=Y, dtype=np.int64).astype(np.int32)
+    token_in = np.arange(Y, dtype=np.int32) if token_ids else None
+    return dict(expert_ids=expert, layer_id=int(layer_id), token_data=token_data,
+                row_stride=int(row_stride), scales=scales, session_in=session_in,
+                micro_in=micro_in, token_in=token_in, expertNum=int(E), A=int(A), BS=int(BS),
+                K1=int(K1), H=int(H), tokenDtype=int(dtype), layerNum=int(layerNum), Y=int(Y))
+
+
+# ---------------------------------------------------------------------------
+# Unpermute inputs
+# ---------------------------------------------------------------------------
+
+def _softmax_rows(logits: np.ndarray, keep: np.ndarray) -> np.ndarray:
+    """Softmax in float64 over the kept entries of each row, 0 elsewhere."""
+    z = np.where(keep, logits, -np.inf)
+    zmax = np.max(z, axis=1, keepdims=True)
+    zmax = np.where(np.isfinite(zmax), zmax, 0.0)
+    e = np.where(keep, np.exp(z - zmax), 0.0)
+    s = e.sum(axis=1, keepdims=True)
+    return np.where(s > 0, e / np.where(s > 0, s, 1.0), 0.0)
+
+
+def make_unpermute_topk(*, T: int, k: int, Eu: int, H: int, dtype: int, probs_dtype: int | None,
+                        choices=(6, 7, 8), seed: int = 1, rows: int | None = None) -> dict:
+    """Not-padded (slot layout) inputs: each token picks n ~ U(choices)
+    experts, the top-n of N(0,1) logits (ties to the lower expert id).
+    permutedTokens rows are the expert-major order of the (token, expert)
+    pairs, as the permute step that precedes the unpermute lays them out;
+    sortedIndices[t*k + j] = row of t's j-th chosen expert (ascending expert
+    id), -1 for unused slots. probs = softmax over the chosen experts, 0
+    elsewhere (None -> no probs)."""
+    rng = _rng(seed, _TAG_ROUTE)
+    nsel = rng.choice(np.asarray(choices, dtype=np.int64), size=T)
+    logits = rng.standard_normal((T, Eu))
+    order = np.argsort(-logits, axis=1, kind="stable")
+    keep = np.zeros((T, Eu), dtype=bool)
+    for t in range(T):
+        keep[t, order[t, :nsel[t]]] = True
+    routing = keep.astype(np.int8)
+    # rows: pairs ordered by (expert, token)
+    tt, ee = np.nonzero(keep)                      # row-major: by token, then expert
+    pair_order = np.lexsort((tt, ee))              # by expert, then token
+    row_of_pair = np.empty(len(tt), dtype=np.int64)
+    row_of_pair[pair_order] = np.arange(len(tt))
+    sorted_idx = np.full(T * k, -1, dtype=np.int32)
+    slot = np.zeros(T, dtype=np.int64)
+    for p in range(len(tt)):                       # pairs of a token come in ascending expert id
+        t = tt[p]
+        sorted_idx[t * k + slot[t]] = row_of_pair[p]
+        slot[t] += 1
+    nrows = T * k if rows is None else rows
+    permuted = normal_rows(nrows, H, dtype, seed)
+    probs = None
+    if probs_dtype is not None:
+        p64 = _softmax_rows(logits, keep)
+        probs = _to_storage(p64.astype(np.float32), probs_dtype)
+    return dict(permuted=permuted, sortedIndices=sorted_idx, routingMap=routing, probs=probs,
+                permutedRows=int(nrows), H=int(H), tokenDtype=int(dtype), n=int(T * k),
+                probsDtype=int(probs_dtype if probs_dtype is not None else dtype), T=int(T),
+                Eu=int(Eu), padded=0)
+
+
+def make_unpermute_padded(*, T: int, Eu: int, k: int, H: int, dtype: int, probs_dtype: int | None,
+                          mult: int = 37, seed: int = 3) -> dict:
+    """Padded (expert capacity) inputs with balanced routing: token t goes to
+    experts (mult*t + (Eu/k)*j) mod Eu for j < k, so with Eu a power of two,
+    mult odd and T a multiple of Eu every expert gets capacity = T*k/Eu tokens.
+    sortedIndices[e*capacity + r] = r-th smallest token routed to e. probs =
+    Dirichlet(1) over the token's k experts (normalised Exp(1) draws)."""
+    step = Eu // k
+    routing = np.zeros((T, Eu), dtype=np.int8)
+    t = np.arange(T)
+    for j in range(k):
+        routing[t, (mult * t + step * j) % Eu] = 1
+    counts = routing.sum(axis=0)
+    cap = int(counts.max())
+    sorted_idx = np.full(Eu * cap, -1, dtype=np.int32)
+    for e in range(Eu):
+        toks = np.nonzero(routing[:, e])[0]
+        sorted_idx[e * cap:e * cap + len(toks)] = toks
+    permuted = normal_rows(Eu * cap, H, dtype, seed)
+    probs = None
+    if probs_dtype is not None:
+        g = _rng(seed, _TAG_PROBS).exponential(1.0, size=(T, Eu))
+        g = np.where(routing != 0, g, 0.0)
+        p64 = g / g.sum(axis=1, keepdims=True)
+        probs = _to_storage(p64.astype(np.float32), probs_dtype)
+    return dict(permuted=permuted, sortedIndices=sorted_idx, routingMap=routing, probs=probs,
+                permutedRows=int(Eu * cap), H=int(H), tokenDtype=int(dtype), n=int(Eu * cap),
+                probsDtype=int(probs_dtype if probs_dtype is not None else dtype), T=int(T),
+                Eu=int(Eu), padded=1, capacity=cap)
+
+
+def make_roundtrip_probs(*, T: int, k: int, slot_unmasked: np.ndarray, probs_dtype: int,
+                         seed: int = 4) -> tuple[np.ndarray, np.ndarray]:
+    """Routing map and probs of the round trip, with one column per slot of a
+    token: routingMap[t, j] = slot t*k+j is unmasked; probs = softmax of
+    N(0,1) logits over the k slots of the token."""
+    routing = slot_unmasked.reshape(T, k).astype(np.int8)
+    logits = _rng(seed, _TAG_PROBS).standard_normal((T, k))
+    p64 = _softmax_rows(logits, np.ones((T, k), dtype=bool))
+    return routing, _to_storage(p64.astype(np.float32), probs_dtype)
+
+
+# ---------------------------------------------------------------------------
+# The five workloads (sizes and distributions of the pages' workloads)
+# ---------------------------------------------------------------------------
+
+BATCHING_TINY = dict(A=2, BS=8, K1=3, E=8, H=128, dtype=DT_F16, layerNum=1, layer_id=0,
+                     ids="uniform", mask=0.10, session=2, micro=4, token_ids=True, seed=0)
+BATCHING_INT8_DECODE = dict(A=64, BS=32, K1=9, E=256, H=7168, dtype=DT_INT8, layerNum=1,
+                            layer_id=0, ids="zipf", zipf_s=1.1, mask=0.15, session=64,
+                            micro=64, token_ids=True, seed=2)
+UNPERMUTE_TOPK = dict(T=4096, k=8, Eu=64, H=4096, dtype=DT_BF16, probs_dtype=DT_BF16, seed=1)
+UNPERMUTE_PADDED = dict(T=16384, Eu=128, k=4, H=4096, dtype=DT_F16, probs_dtype=DT_F32, seed=3)
+ROUNDTRIP_BATCHING = dict(A=256, BS=64, K1=9, E=1024, H=7168, dtype=DT_BF16, layerNum=4,
+                          layer_id=2, ids="zipf", zipf_s=1.2, mask=0.05, session=256, micro=64,
+                          token_ids=True, seed=4)
+ROUNDTRIP_PROBS_DTYPE = DT_BF16
