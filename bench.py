@@ -1,0 +1,496 @@
+"""Benchmark of the MoE expert-grouped token reorder on GB300.
+
+One step = one pass of the whole hot path over one batch of synthetic input,
+the full-scale round trip: FFN-worker batching of Y = 256*64*9 = 147456 slots
+(expertNum 1024 over 4 layers, layer 2, H = 7168 bf16, Zipf(1.2) expert ids,
+5% masked), then the not-padded unpermute with probs of its output y back to
+16384 tokens x topK 9.
+
+Prints ONE JSON line (rank 0). `value` is the effective HBM bandwidth of the
+step (algorithmic bytes read + written / device time) over all ranks;
+`tokens_per_s` the tokens the step processes per second. Inputs are larger
+than L2 (2.1 GB of token rows per step), so no L2 flush is needed.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the program the kernels are checked
+against) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as w  # noqa: E402
+
+METRIC = "permute/unpermute effective HBM GB/s (% of ~8 TB/s peak) and tokens/s, 1 GB300"
+WORKLOAD = ("full-scale round trip: batching A=256 BS=64 topK+1=9 (Y=147456) expertNum=1024 "
+            "layerNum=4 layer_id=2 H=7168 bf16 Zipf(1.2) 5% masked, then not-padded unpermute "
+            "with probs T=16384 topK=9 bf16")
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "traffic.json")
+FALLBACK_HBM_GBS = 6800.0
+CSRC = os.path.join(ROOT, "unpermute_stable_counting_gb300", "csrc")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample-attn", type=int, default=32,
+                    help="attention workers (A) of the oracle's bounded sample (full workload: 256)")
+    ap.add_argument("--small", action="store_true", help="a small case of the same workload (profiling)")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------------------
+# Workload and its algorithmic bytes
+# ---------------------------------------------------------------------------
+
+def workload_spec(small=False, attn=None):
+    spec = dict(w.ROUNDTRIP_BATCHING)
+    if small:
+        spec["A"] = 32  # Y = 18432 slots, 264 MB of token rows: still larger than L2
+    if attn is not None:
+        spec["A"] = attn
+    return spec
+
+
+def make_host_inputs(spec):
+    inp = w.make_batching(**spec)
+    T, k = spec["A"] * spec["BS"], spec["K1"]
+    El = spec["E"] // max(spec["layerNum"], 1)
+    unmasked = (inp["expert_ids"] >= 0) & (inp["expert_ids"] < El)
+    rmap, probs = w.make_roundtrip_probs(T=T, k=k, slot_unmasked=unmasked,
+                                         probs_dtype=w.ROUNDTRIP_PROBS_DTYPE, seed=spec["seed"])
+    return inp, rmap, probs, int(unmasked.sum())
+
+
+def algorithmic_bytes(spec, U, V):
+    """Bytes each step must read and write (inputs once, outputs once)."""
+    Y = spec["A"] * spec["BS"] * spec["K1"]
+    H, E = spec["H"], spec["E"]
+    s = w.ELEM_BYTES[spec["dtype"]]
+    T, k = spec["A"] * spec["BS"], spec["K1"]
+    ps = w.ELEM_BYTES[w.ROUNDTRIP_PROBS_DTYPE]
+    row = H * s
+    # batching: keys, the U gathered rows, session/micro/token id lookups; y rows,
+    # four int32 id outputs, the slot -> row map, group_list, actual_token_num
+    b_read = Y * 4 + U * row + U * 12
+    b_write = U * row + Y * 16 + Y * 4 + E * 16 + 8
+    # unpermute: sortedIndices, the V contributing rows, routing map and probs;
+    # the token outputs, outIndex, permuteTokenId, permuteProbs
+    u_read = T * k * 4 + V * row + T * k * (1 + ps)
+    u_write = T * row + T * k * (8 + ps)
+    gather = U * (2 * row + 4)                    # batching row-gather kernel
+    reduce_ = V * row + T * row + T * k * (4 + ps)  # unpermute gather-reduce kernel
+    return dict(batching=b_read + b_write, unpermute=u_read + u_write, total=b_read + b_write + u_read + u_write,
+                gather_kernel=gather, reduce_kernel=reduce_, tokens=T, slots=Y)
+
+
+def sort_passes(key_range):
+    if key_range <= 4096:
+        return 1
+    bits = int(np.ceil(np.log2(key_range)))
+    return (bits + 11) // 12
+
+
+def launches_per_step(spec):
+    Y = spec["A"] * spec["BS"] * spec["K1"]
+    batching = 4  # rank, prefix, scatter, gather
+    unpermute = 3 + 3 * sort_passes(Y + 1) + 1  # maskedSelect (3), sort passes, reduce
+    return batching + unpermute
+
+
+# ---------------------------------------------------------------------------
+# Peaks, clocks, ncu traffic
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    try:
+        with open(PEAKS_FILE) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def source_digest(files):
+    """Digest of the kernel source files a profile was taken on."""
+    h = hashlib.sha256()
+    for name in sorted(files):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel, units):
+    """DRAM bytes (read + write) per launch from the committed ncu summary,
+    scaled to `units` rows, or None if absent or if the kernel's source files
+    changed since the counters were taken."""
+    try:
+        with open(TRAFFIC_FILE) as f:
+            e = json.load(f)["kernels"][kernel]
+        if e.get("source_digest") != source_digest(e["files"]):
+            return None
+        return float(e["dram_bytes_per_unit"]) * units
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, local_rank):
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        ids = [v.strip() for v in vis.split(",") if v.strip()]
+        self.index = ids[local_rank] if local_rank < len(ids) else str(local_rank)
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 8:
+                continue
+            try:
+                sm.append(float(p[0]))
+                mx.append(float(p[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, p[4:8]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+# Distributed plumbing (replicas only: no data-path collective)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Largest value over all ranks (the timing rule: the slowest rank)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_value(bytes_per_rank: float, world: int, max_seconds_per_step: float) -> float:
+    """Whole-job effective GB/s: bytes all ranks moved / the slowest rank's time."""
+    return bytes_per_rank * world / max_seconds_per_step / 1e9
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (baseline and reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_step(spec, inp, rmap, probs):
+    import oracle
+    T, k = spec["A"] * spec["BS"], spec["K1"]
+    t0 = time.perf_counter()
+    b = oracle.batching(inp)
+    u = dict(permuted=b["y"], sortedIndices=b["sortedIndices"], routingMap=rmap, probs=probs,
+             permutedRows=inp["Y"], H=inp["H"], tokenDtype=inp["tokenDtype"], n=T * k,
+             probsDtype=w.ROUNDTRIP_PROBS_DTYPE, T=T, Eu=k, padded=0)
+    oracle.unpermute(u)
+    return time.perf_counter() - t0
+
+
+def contributing_rows(spec, inp, probs):
+    """V: slots whose row the unpermute reads (valid index and nonzero prob)."""
+    El = spec["E"] // max(spec["layerNum"], 1)
+    unmasked = (inp["expert_ids"] >= 0) & (inp["expert_ids"] < El)
+    # the not-padded weight of slot i is the i-th maskedSelect value (expert-major order)
+    T, k = spec["A"] * spec["BS"], spec["K1"]
+    pv = probs.reshape(T, k).T[unmasked.reshape(T, k).T]
+    nz = np.zeros(T * k, dtype=bool)
+    nz[:pv.size] = (pv != 0)
+    return int((unmasked & nz).sum())
+
+
+def cpu_baseline(spec, inp, rmap, probs, ab):
+    """The oracle, as it stands, on one step of the same inputs (rank 0)."""
+    import oracle
+    oracle.build()
+    dt = oracle_step(spec, inp, rmap, probs)
+    return {"value": ab["total"] / dt / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "tokens_per_s": ab["tokens"] / dt, "seconds": dt,
+            "sample": (f"one step of the same workload (A={spec['A']}, Y={ab['slots']} slots, "
+                       f"{ab['tokens']} tokens, H={spec['H']}) on the single-threaded oracle, "
+                       f"input generation excluded")}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    spec = workload_spec(attn=args.cpu_sample_attn)
+    inp, rmap, probs, U = make_host_inputs(spec)
+    V = contributing_rows(spec, inp, probs)
+    ab = algorithmic_bytes(spec, U, V)
+    for _ in range(args.warmup):
+        oracle_step(spec, inp, rmap, probs)
+    times = [oracle_step(spec, inp, rmap, probs) for _ in range(args.steps)]
+    total = sum(times)
+    value = ab["total"] * args.steps / total / 1e9
+    sample = (f"each step: the round trip with A={spec['A']} attention workers instead of 256 "
+              f"(Y={ab['slots']} slots, {ab['tokens']} tokens, H=7168) on the single-threaded CPU oracle")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "sample": sample},
+            "tokens_per_s": ab["tokens"] * args.steps / total,
+            "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    import unpermute_stable_counting_gb300 as usc
+    from unpermute_stable_counting_gb300 import _build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build_library()
+
+    spec = workload_spec(small=args.small)
+    inp, rmap, probs, U = make_host_inputs(spec)
+    V = contributing_rows(spec, inp, probs)
+    ab = algorithmic_bytes(spec, U, V)
+    Y, H, E = inp["Y"], inp["H"], inp["expertNum"]
+    T, k = spec["A"] * spec["BS"], spec["K1"]
+    shape = (inp["A"], inp["BS"], inp["K1"], H)
+    pdt = w.ROUNDTRIP_PROBS_DTYPE
+
+    # pinned host copies (e2e) and device-resident inputs
+    def pinned(a):
+        t = torch.from_numpy(np.ascontiguousarray(a))
+        return t.pin_memory()
+
+    h_ids, h_td = pinned(inp["expert_ids"]), pinned(inp["token_data"])
+    h_sess, h_micro, h_tok = pinned(inp["session_in"]), pinned(inp["micro_in"]), pinned(inp["token_in"])
+    h_rmap, h_probs = pinned(rmap), pinned(probs.view(np.int16))
+    d = {n: t.to(dev) for n, t in dict(ids=h_ids, td=h_td, sess=h_sess, micro=h_micro, tok=h_tok,
+                                       rmap=h_rmap, probs=h_probs).items()}
+    d_td = d["td"].view(torch.bfloat16).view(Y, H)
+    d_probs = d["probs"].view(torch.bfloat16).view(T, k)
+
+    bout = usc.batching_outputs(Y, H, E, inp["tokenDtype"], dev, with_sorted_indices=True)
+    uout = usc.unpermute_outputs(T, H, T * k, inp["tokenDtype"], pdt, dev)
+    bws = torch.empty(usc.batching_workspace_size(E, shape, inp["tokenDtype"], inp["layerNum"]),
+                      dtype=torch.uint8, device=dev)
+    uws = torch.empty(usc.unpermute_workspace_size(Y, H, inp["tokenDtype"], T * k, True, pdt, T, k,
+                                                   False), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(td=d_td, ids=d["ids"], sess=d["sess"], micro=d["micro"], tok=d["tok"], rm=d["rmap"],
+             pr=d_probs):
+        usc.ffnwb_batching(ids, td, sess, micro, expert_num=E, max_out_shape=shape,
+                           token_dtype=inp["tokenDtype"], layer_num=inp["layerNum"],
+                           layer_id=inp["layer_id"], token_ids=tok, with_sorted_indices=True,
+                           out=bout, workspace=bws, stream=stream)
+        usc.moe_unpermute(bout["y"], bout["sortedIndices"], rm, pr, padded_mode=False, out=uout,
+                          workspace=uws, stream=stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- device-resident timing ------------------------------------------------
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    if clocks is not None:
+        clocks["window"] = "warm-up and timed steps"
+    sec_step = e0.elapsed_time(e1) / 1e3 / args.steps
+    sec_step = max_over_ranks(sec_step, world, dev)
+
+    # ---- per-phase kernel times (library phase events on the launch stream) ----
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+    phase = {p: [] for p in range(4)}
+    usc.profile_set_events(ev)
+    try:
+        for _ in range(args.steps):
+            step()
+            torch.cuda.synchronize()
+            for p in range(4):
+                phase[p].append(ev[2 * p].elapsed_time(ev[2 * p + 1]) / 1e3)
+    finally:
+        usc.profile_set_events(None)
+    ph = {p: statistics.mean(v) for p, v in phase.items()}
+
+    # ---- end to end through host buffers -----------------------------------
+    e2e = None
+    if not args.no_e2e:
+        h_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
+                 for n, t in uout.items() if t is not None}
+        h_bout = {n: torch.empty(bout[n].shape, dtype=bout[n].dtype).pin_memory()
+                  for n in ("groupList", "actualTokenNum", "sessionIds", "microBatchIds",
+                            "tokenIds", "expertOffsets")}
+        ins = [(d["ids"], h_ids), (d["td"], h_td), (d["sess"], h_sess), (d["micro"], h_micro),
+               (d["tok"], h_tok), (d["rmap"], h_rmap), (d["probs"], h_probs)]
+        h2d = sum(h.numel() * h.element_size() for _, h in ins)
+        outs = [(uout[n], h_out[n]) for n in h_out] + [(bout[n], h_bout[n]) for n in h_bout]
+        d2h = sum(h.numel() * h.element_size() for _, h in outs)
+
+        def e2e_step():
+            for dd, hh in ins:
+                dd.copy_(hh, non_blocking=True)
+            step()
+            for dd, hh in outs:
+                hh.copy_(dd, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        barrier()
+        n_e2e = max(3, min(args.steps, 10))
+        e0.record(stream)
+        for _ in range(n_e2e):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_sec = max_over_ranks(e0.elapsed_time(e1) / 1e3 / n_e2e, world, dev)
+        e2e = {"value": aggregate_value(ab["total"], world, e2e_sec), "unit": "GB/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_sec * 1e3,
+               "steps": n_e2e}
+
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = hbm_peak()
+    gather_gbs = ab["gather_kernel"] / ph[1] / 1e9
+    reduce_gbs = ab["reduce_kernel"] / ph[3] / 1e9
+    traffic = ncu_traffic("batching_gather_kernel", U)
+    value = aggregate_value(ab["total"], world, sec_step)
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": sec_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD if not args.small else WORKLOAD + " (A=32 small case)",
+                   "l2": "inputs larger than L2 (2.1 GB of token rows per step); no flush",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "U_rows": U, "V_rows": V, "alg_bytes_per_step": ab["total"]},
+        "tokens_per_s": ab["tokens"] * world / sec_step,
+        "frac_of_hbm_peak": value / world / peak,
+        "roofline": {"bound": "hbm", "kernel": "batching_gather_kernel", "achieved": gather_gbs,
+                     "peak": peak, "unit": "GB/s", "frac": gather_gbs / peak,
+                     "peak_source": f"{peak_kind} hbm_gbs", "traffic": traffic,
+                     "alg_bytes_per_launch": ab["gather_kernel"]},
+        "kernels": {
+            "batching_index_ms": ph[0] * 1e3, "batching_gather_ms": ph[1] * 1e3,
+            "batching_gather_gbs": gather_gbs,
+            "unpermute_index_ms": ph[2] * 1e3, "unpermute_reduce_ms": ph[3] * 1e3,
+            "unpermute_reduce_gbs": reduce_gbs, "unpermute_reduce_frac": reduce_gbs / peak,
+            "batching_gbs": ab["batching"] / (ph[0] + ph[1]) / 1e9,
+            "unpermute_gbs": ab["unpermute"] / (ph[2] + ph[3]) / 1e9},
+        "gpu_launches": launches_per_step(spec) * args.steps,
+        "clocks": clocks,
+        "e2e": e2e,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        try:
+            line["cpu_baseline"] = cpu_baseline(spec, inp, rmap, probs, ab)
+        except Exception as ex:  # the oracle needs g++; report rather than fail the bench
+            line["cpu_baseline"] = {"value": None, "error": str(ex)[:200]}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

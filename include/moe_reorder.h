@@ -1,0 +1,254 @@
+/*
+ * moe_reorder.h -- C ABI of the GB300 MoE expert-grouped token reorder.
+ *
+ * Two operations, each a two-stage call in the style of the pages' aclnn
+ * interfaces (a get-workspace-size call that validates and sizes, then an
+ * execute call that enqueues on a stream):
+ *
+ *   ffnwb_batching  -- "aclnnFfnWorkerBatching": 功能说明 (steps 2-4 and the
+ *                      计算公式), 参数说明 (parameter table), 约束说明.
+ *   moe_unpermute   -- "MoeTokenUnpermuteWithRoutingMap 算子全解析":
+ *                      功能说明与计算公式 (derived sizes, four branches),
+ *                      参数说明 / 补充说明 (shapes, ranges), 约束说明,
+ *                      返回值与错误码, Kernel 实现 (skip rules, fp32 math).
+ *
+ * Conventions shared by every entry point
+ *  - Pointers named as device pointers must point to device memory of the
+ *    current CUDA device; pointers named host pointers to host memory.
+ *  - The caller owns and frees every buffer, including the workspace. The
+ *    library allocates no device memory and keeps no per-call state.
+ *  - Execute calls are asynchronous on `stream` (a cudaStream_t; NULL = the
+ *    legacy default stream). Outputs are valid once the caller synchronises
+ *    the stream. Nothing is read back to the host.
+ *  - Argument errors are detected on the host before anything is enqueued;
+ *    the call then returns the error and enqueues nothing. Errors that the
+ *    CUDA runtime reports at launch return MR_ERR_CUDA.
+ *  - Outputs must not alias inputs or each other.
+ *  - Results are deterministic: identical inputs give identical bits.
+ */
+#ifndef MOE_REORDER_H
+#define MOE_REORDER_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t mr_status;
+
+/* Status codes. The first three carry the numeric values of the pages'
+ * aclnnStatus codes ("aclnnFfnWorkerBatching" 返回值 table;
+ * "MoeTokenUnpermuteWithRoutingMap 算子全解析" 返回值与错误码). */
+#define MR_OK                 0
+#define MR_ERR_PARAM_NULLPTR  161001 /* a required pointer is NULL */
+#define MR_ERR_PARAM_INVALID  161002 /* dtype / shape / range out of the supported set */
+#define MR_ERR_INNER          561103 /* topK_num > 512, or a probs shape out of range */
+#define MR_ERR_CUDA           561001 /* the CUDA runtime reported an error */
+#define MR_ERR_WORKSPACE      561002 /* workspaceSize smaller than required */
+#define MR_ERR_UNSUPPORTED    561003 /* a valid mode this library does not implement */
+
+/* Element types (tokenDtype / probsDtype). 0..2 are the batching page's
+ * tokenDtype values; 3 is FP32 (allowed for the unpermute tensors). */
+#define MR_DTYPE_F16   0
+#define MR_DTYPE_BF16  1
+#define MR_DTYPE_INT8  2 /* int8 rows with an fp32 dynamic scale */
+#define MR_DTYPE_F32   3
+
+/* Sentinel-free limits from the pages' constraint tables. */
+#define MR_MAX_EXPERT_NUM 8192 /* expertNum in (0, 8192] */
+#define MR_MAX_A          1024 /* A in (0, 1024] */
+#define MR_MAX_TOPK1      64   /* topK+1 in (0, 64] */
+#define MR_MAX_TOPK_NUM   512  /* unpermute topK_num <= 512 */
+
+/* ------------------------------------------------------------------------ */
+/* FFN-worker batching                                                      */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * ffnwb_batching_get_workspace_size
+ *   "aclnnFfnWorkerBatching", 参数说明 (first-stage call) and 约束说明.
+ *   Validates the attributes and returns, in *workspaceSize (host pointer),
+ *   the bytes of device workspace ffnwb_batching needs.
+ *
+ *   expertNum    experts on this device over all layers, in (0, 8192].
+ *   maxOutShape  host pointer to 4 int64: {A, BS, topK+1, H}; A in (0,1024],
+ *                BS > 0, topK+1 in (0,64], H > 0. Y = A*BS*(topK+1) must be
+ *                below 2^31.
+ *   tokenDtype   MR_DTYPE_F16, MR_DTYPE_BF16 or MR_DTYPE_INT8.
+ *   needSchedule 0 (batching only). 1 (scan the ScheduleContext first) is a
+ *                valid value on the page that this library does not
+ *                implement: MR_ERR_UNSUPPORTED.
+ *   layerNum     in [0, expertNum]; expertNum must be a multiple of
+ *                max(layerNum, 1).
+ *   Returns MR_OK, MR_ERR_PARAM_NULLPTR (maxOutShape or workspaceSize NULL),
+ *   MR_ERR_PARAM_INVALID or MR_ERR_UNSUPPORTED.
+ */
+mr_status ffnwb_batching_get_workspace_size(int64_t expertNum, const int64_t* maxOutShape,
+                                            int64_t tokenDtype, int64_t needSchedule,
+                                            int64_t layerNum, uint64_t* workspaceSize);
+
+/*
+ * ffnwb_batching
+ *   "aclnnFfnWorkerBatching", 功能说明 steps 2-4 and 计算公式:
+ *     gather_idx, _ = sort(expert_ids_in)        (masked slots keyed last)
+ *     y[i] = token_data[gather_idx[i]]           (+ dynamic scale, INT8)
+ *     group_list[e] = [expert_id_e, expert_token_num_e]
+ *     actual_token_num = sum_e expert_token_num_e
+ *   The page's ScheduleContext is replaced by flat arrays of the Y slots.
+ *
+ *   Inputs (device pointers unless noted; Y = A*BS*(topK+1) slots):
+ *   expertIds       int32 [Y]: local expert id of each slot. A slot is masked
+ *                   when its id is outside [0, E_l), E_l = expertNum /
+ *                   max(layerNum,1) (e.g. INT32_MAX).
+ *   layerId         the layer of every slot of this call, in
+ *                   [0, max(layerNum,1)). Slot key = layerId*E_l + id.
+ *   tokenData       Y rows, row s at tokenData + s*tokenRowStride bytes.
+ *                   FP16/BF16: H values. INT8: H int8 values, and (when
+ *                   scales is NULL) the fp32 scale in the 4 bytes right
+ *                   after them.
+ *   tokenRowStride  bytes between rows; >= H*elem (INT8 interleaved: >= H+4).
+ *   scales          INT8 only, nullable: fp32 scale of slot s at
+ *                   scales + s*scaleStride bytes.
+ *   scaleStride     bytes between scales (ignored when scales is NULL).
+ *   sessionIdsIn,
+ *   microBatchIdsIn int32 [Y]: session / micro-batch id of each slot.
+ *   tokenIdsIn      int32 [Y], nullable: token id of each slot; NULL means
+ *                   the slot index.
+ *   expertNum, maxOutShape (host), tokenDtype, needSchedule, layerNum:
+ *                   as in ffnwb_batching_get_workspace_size.
+ *   Outputs (device pointers; rows are in stable sort order of the key):
+ *   y               [Y, H] of tokenDtype, dense rows. Rows i < U are written
+ *                   (U = unmasked slots); rows i >= U are left untouched.
+ *   groupList       int64 [expertNum, 2]: row r = [key, count] of the r-th
+ *                   distinct present key in ascending order; remaining rows
+ *                   [0, 0].
+ *   sessionIds, microBatchIds, tokenIds, expertOffsets
+ *                   int32 [Y]: ids of the slot in row i, and i minus the first
+ *                   row of its key; -1 for rows i >= U.
+ *   dynamicScale    float [Y]: INT8 only (must be NULL otherwise); rows i < U.
+ *   actualTokenNum  int64 [1]: U.
+ *   sortedIndicesOut int32 [Y], nullable: row of slot s in y, -1 if masked --
+ *                   the sortedIndices of the unpermute's non-padded layout.
+ *   workspace       device memory of at least the size the first stage
+ *                   returned for the same attributes.
+ *   stream          cudaStream_t.
+ *   Returns MR_OK, MR_ERR_PARAM_NULLPTR, MR_ERR_PARAM_INVALID,
+ *   MR_ERR_UNSUPPORTED, MR_ERR_WORKSPACE or MR_ERR_CUDA.
+ */
+mr_status ffnwb_batching(const int32_t* expertIds, int32_t layerId, const void* tokenData,
+                         int64_t tokenRowStride, const void* scales, int64_t scaleStride,
+                         const int32_t* sessionIdsIn, const int32_t* microBatchIdsIn,
+                         const int32_t* tokenIdsIn, int64_t expertNum, const int64_t* maxOutShape,
+                         int64_t tokenDtype, int64_t needSchedule, int64_t layerNum, void* y,
+                         int64_t* groupList, int32_t* sessionIds, int32_t* microBatchIds,
+                         int32_t* tokenIds, int32_t* expertOffsets, float* dynamicScale,
+                         int64_t* actualTokenNum, int32_t* sortedIndicesOut, void* workspace,
+                         uint64_t workspaceSize, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Routing-map unpermute                                                    */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * moe_unpermute_get_workspace_size
+ *   "MoeTokenUnpermuteWithRoutingMap 算子全解析", 调用说明 (first stage),
+ *   功能说明与计算公式 (derived sizes), 约束说明, 返回值与错误码.
+ *
+ *   permutedRows      rows of permutedTokens (size(0)).
+ *   hidden            H = permutedTokens.size(1) > 0.
+ *   tokenDtype        MR_DTYPE_F16, MR_DTYPE_BF16 or MR_DTYPE_F32.
+ *   numSortedIndices  n = len(sortedIndices).
+ *   hasProbs          1 if probs and routingMap are given, else 0.
+ *   probsDtype        tokenDtype or MR_DTYPE_F32 (ignored without probs).
+ *   numTokens         T = probs.size(0) = routingMap.size(0) (with probs).
+ *   numExperts        probs.size(1) (with probs).
+ *   paddedMode        0 or 1.
+ *   restoreShape      host pointer, nullable: {T, H} of the output. Required
+ *                     without probs (it gives T); must agree with numTokens
+ *                     and hidden otherwise.
+ *   Derived: topK_num = permutedRows / T. Not padded: n == T*topK_num.
+ *   Padded: n == permutedRows, capacity = n / numExperts (with probs n must be
+ *   a multiple of numExperts).
+ *   Returns MR_OK, MR_ERR_PARAM_NULLPTR, MR_ERR_PARAM_INVALID or MR_ERR_INNER
+ *   (topK_num > 512, or the probs shape out of range).
+ */
+mr_status moe_unpermute_get_workspace_size(int64_t permutedRows, int64_t hidden,
+                                           int32_t tokenDtype, int64_t numSortedIndices,
+                                           int32_t hasProbs, int32_t probsDtype,
+                                           int64_t numTokens, int64_t numExperts,
+                                           int32_t paddedMode, const int64_t* restoreShape,
+                                           uint64_t* workspaceSize);
+
+/*
+ * moe_unpermute
+ *   "MoeTokenUnpermuteWithRoutingMap 算子全解析", 功能说明与计算公式:
+ *   (1) probs, padded:     permuteProbs[i] = probs[sortedIndices[i], i // capacity];
+ *                          permuteTokenId, outIndex = sortedIndices.sort();
+ *                          out[permuteTokenId[i]] += permuted[outIndex[i]] * permuteProbs[outIndex[i]]
+ *   (2) probs, not padded: permuteProbs = probs.T.maskedSelect(routingMap.T);
+ *                          out[i // topK_num] += permuted[sortedIndices[i]] * permuteProbs[i]
+ *   (3), (4): the same without probs.
+ *   A term is skipped unless its index is valid (not padded:
+ *   0 <= idx < permutedRows; padded: 0 <= token < T) and, with probs, its
+ *   prob is nonzero. Terms are cast to fp32, multiplied by the fp32 prob,
+ *   rounded, and added in fp32 in ascending slot (not padded) or row
+ *   (padded) order; the sum is cast back with round-to-nearest-even.
+ *   Tokens without a term get 0.
+ *
+ *   Inputs (device pointers):
+ *   permutedTokens  [permutedRows, H] of tokenDtype.
+ *   sortedIndices   int32 [n].
+ *   routingMap      int8/bool [T, numExperts], nullable; NULL iff probs NULL.
+ *   probs           [T, numExperts] of probsDtype, nullable.
+ *   (shape arguments as in moe_unpermute_get_workspace_size)
+ *   Outputs (device pointers):
+ *   unpermutedTokens [T, H] of tokenDtype.
+ *   outIndex         int32 [n]: positions of the stable ascending sort of
+ *                    sortedIndices. Not padded: invalid entries first.
+ *                    Padded: invalid entries last.
+ *   permuteTokenId   int32 [n]: not padded: outIndex // topK_num; padded: the
+ *                    sorted values (sortedIndices[outIndex[i]]).
+ *   permuteProbs     [n] of probsDtype, required with probs, ignored without:
+ *                    not padded: the maskedSelect values, truncated to n,
+ *                    then zeros; padded: the lookup above, 0 where the index
+ *                    is invalid.
+ *   workspace, workspaceSize, stream: as for ffnwb_batching.
+ *   Returns MR_OK, MR_ERR_PARAM_NULLPTR, MR_ERR_PARAM_INVALID, MR_ERR_INNER,
+ *   MR_ERR_WORKSPACE or MR_ERR_CUDA.
+ */
+mr_status moe_unpermute(const void* permutedTokens, const int32_t* sortedIndices,
+                        const int8_t* routingMap, const void* probs, int64_t permutedRows,
+                        int64_t hidden, int32_t tokenDtype, int64_t numSortedIndices,
+                        int32_t probsDtype, int64_t numTokens, int64_t numExperts,
+                        int32_t paddedMode, const int64_t* restoreShape, void* unpermutedTokens,
+                        int32_t* outIndex, int32_t* permuteTokenId, void* permuteProbs,
+                        void* workspace, uint64_t workspaceSize, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Utilities (no counterpart on the pages)                                  */
+/* ------------------------------------------------------------------------ */
+
+/* Short English text of a status code (static storage). */
+const char* mr_status_string(mr_status status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int32_t mr_version(void);
+
+/*
+ * mr_profile_set_events -- timing aid for benchmarks.
+ *   events: host array of `count` cudaEvent_t handles (count even, <= 16), or
+ *   NULL / 0 to switch timing off. While set, the calling thread's execute
+ *   calls record events[2p] before and events[2p+1] after phase p on their
+ *   stream, phases being: 0 batching index build, 1 batching row gather,
+ *   2 unpermute index work (maskedSelect / probs lookup and the sort),
+ *   3 unpermute gather-reduce. Phases beyond `count/2` are not recorded.
+ *   The setting is per host thread. Returns MR_OK or MR_ERR_PARAM_INVALID.
+ */
+mr_status mr_profile_set_events(void* const* events, int32_t count);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_REORDER_H */

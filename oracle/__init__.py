@@ -10,6 +10,7 @@ arrays through ctypes.
 from __future__ import annotations
 
 import ctypes
+import fcntl
 import os
 import subprocess
 
@@ -38,10 +39,20 @@ def compile_library(src: str, out: str) -> str:
     return out
 
 
+def _stale() -> bool:
+    return not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+
+
 def build(force: bool = False) -> str:
-    """Compile oracle.cpp into liboracle.so (next to it)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        compile_library(_SRC, _LIB)
+    """Compile oracle.cpp into liboracle.so (next to it), one builder at a time."""
+    if force or _stale():
+        with open(os.path.join(_HERE, ".build.lock"), "w") as lk:
+            fcntl.flock(lk, fcntl.LOCK_EX)
+            try:
+                if force or _stale():
+                    compile_library(_SRC, _LIB)
+            finally:
+                fcntl.flock(lk, fcntl.LOCK_UN)
     return _LIB
 
 

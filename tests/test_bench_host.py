@@ -1,0 +1,113 @@
+"""Host logic of bench.py, on the CPU: algorithmic byte counts, launch
+counts, the max-over-ranks timing rule with two gloo ranks, and the
+reference arm's JSON line."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+import workloads as w
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def test_algorithmic_bytes_by_hand():
+    spec = dict(A=1, BS=2, K1=3, E=8, H=4, dtype=w.DT_BF16, layerNum=1)
+    Y, T, k, row = 6, 2, 3, 8
+    U, V = 5, 4
+    ab = bench.algorithmic_bytes(spec, U, V)
+    assert ab["batching"] == (Y * 4 + U * row + U * 12) + (U * row + Y * 16 + Y * 4 + 8 * 16 + 8)
+    assert ab["unpermute"] == (T * k * 4 + V * row + T * k * 3) + (T * row + T * k * 10)
+    assert ab["total"] == ab["batching"] + ab["unpermute"]
+    assert ab["gather_kernel"] == U * (2 * row + 4)
+    assert ab["tokens"] == T and ab["slots"] == Y
+
+
+def test_roundtrip_workload_bytes_are_about_six_gigabytes():
+    spec = bench.workload_spec()
+    Y = spec["A"] * spec["BS"] * spec["K1"]
+    U = int(0.95 * Y)
+    ab = bench.algorithmic_bytes(spec, U, U)
+    assert 3.9e9 < ab["batching"] < 4.2e9
+    assert 2.1e9 < ab["unpermute"] < 2.4e9
+
+
+def test_launch_count():
+    spec = bench.workload_spec()
+    # batching: rank, prefix, scatter, gather; unpermute: maskedSelect (3),
+    # two sort passes of 3 launches (147457 keys -> 18 bits), reduce
+    assert bench.sort_passes(147457) == 2
+    assert bench.sort_passes(4096) == 1
+    assert bench.sort_passes(4097) == 1 + (13 > 12)
+    assert bench.launches_per_step(spec) == 4 + 3 + 6 + 1
+
+
+def test_contributing_rows_counts_valid_nonzero_slots():
+    spec = dict(A=1, BS=2, K1=3, E=4, layerNum=1)
+    inp = dict(expert_ids=np.array([0, 9, 1, 2, 3, 2**31 - 1], np.int32))
+    probs = np.array([[1, 1, 1], [1, 1, 1]], np.uint16)
+    # 4 unmasked slots (0, 2, 3, 4) give 4 maskedSelect values; slot i takes
+    # the i-th value, so slot 4 gets the zero tail and is skipped
+    assert bench.contributing_rows(spec, inp, probs) == 3
+
+
+def _rank(rank, world, port, q):
+    import torch.distributed as dist
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    t = bench.max_over_ranks(0.5 + rank, world)
+    q.put((rank, t, bench.aggregate_value(1e9, world, t)))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def test_max_over_ranks_gloo_two_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    # both ranks see the slowest rank's time; value counts both ranks' bytes
+    assert [r[1] for r in res] == [1.5, 1.5]
+    assert all(abs(r[2] - 2e9 / 1.5 / 1e9) < 1e-9 for r in res)
+
+
+def test_reference_arm_json_line():
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                        "--warmup", "0", "--cpu-sample-attn", "2"], cwd=ROOT, capture_output=True,
+                       text=True, timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "GB/s" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] == 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_print_nothing():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--steps", "1",
+                        "--warmup", "0", "--cpu-sample-attn", "2"], cwd=ROOT, capture_output=True,
+                       text=True, timeout=600, env=env)
+    assert r.returncode == 0 and r.stdout.strip() == ""

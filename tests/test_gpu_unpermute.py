@@ -1,0 +1,145 @@
+"""Unpermute: CUDA path vs the oracle on the same seeded inputs. Index and
+prob outputs bit for bit; unpermutedTokens within the stated tolerance (and,
+by construction of the kernels, bit for bit as well)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as w
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+from _gpu_util import assert_unpermute_equal, run_unpermute, unpermute_numpy  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def check(inp, **kw):
+    ref = oracle.unpermute(inp)
+    got = unpermute_numpy(run_unpermute(inp, **kw), inp)
+    assert_unpermute_equal(got, ref, inp)
+    return got, ref
+
+
+def test_page_example_padded():
+    inp = dict(permuted=np.ones((2, 2), np.float32), sortedIndices=np.array([1, 1], np.int32),
+               routingMap=np.ones((2, 2), np.int8), probs=np.ones((2, 2), np.float32),
+               permutedRows=2, H=2, tokenDtype=3, n=2, probsDtype=3, T=2, Eu=2, padded=1)
+    got, _ = check(inp)
+    assert got["unpermuted"].tolist() == [[0.0, 0.0], [2.0, 2.0]]
+
+
+def test_topk_workload():
+    check(w.make_unpermute_topk(**w.UNPERMUTE_TOPK))
+
+
+def test_padded_workload():
+    check(w.make_unpermute_padded(**w.UNPERMUTE_PADDED))
+
+
+COMBOS = [(0, 0), (0, 3), (1, 1), (1, 3), (3, 3)]
+
+
+@pytest.mark.parametrize("dt,pdt", COMBOS)
+@pytest.mark.parametrize("with_probs", [True, False])
+def test_not_padded_dtypes(dt, pdt, with_probs):
+    inp = w.make_unpermute_topk(T=300, k=6, Eu=24, H=136, dtype=dt,
+                                probs_dtype=pdt if with_probs else None, choices=(1, 3, 6),
+                                seed=dt * 10 + pdt)
+    check(inp)
+
+
+@pytest.mark.parametrize("dt,pdt", COMBOS)
+@pytest.mark.parametrize("with_probs", [True, False])
+def test_padded_dtypes(dt, pdt, with_probs):
+    inp = w.make_unpermute_padded(T=512, Eu=32, k=4, H=72, dtype=dt,
+                                  probs_dtype=pdt if with_probs else None, mult=5,
+                                  seed=dt * 10 + pdt)
+    check(inp)
+
+
+@pytest.mark.parametrize("H", [1, 7, 9, 33])
+@pytest.mark.parametrize("padded", [0, 1])
+def test_odd_hidden_scalar_path(H, padded):
+    if padded:
+        inp = w.make_unpermute_padded(T=64, Eu=16, k=4, H=H, dtype=1, probs_dtype=3, mult=3, seed=H)
+    else:
+        inp = w.make_unpermute_topk(T=70, k=5, Eu=12, H=H, dtype=0, probs_dtype=0,
+                                    choices=(2, 5), seed=H)
+    check(inp)
+
+
+def test_invalid_indices_duplicates_and_zero_probs():
+    rng = np.random.default_rng(5)
+    inp = w.make_unpermute_topk(T=257, k=7, Eu=20, H=64, dtype=1, probs_dtype=3, choices=(1, 4, 7),
+                                seed=5)
+    si = inp["sortedIndices"]
+    pick = rng.random(si.size) < 0.1
+    si[pick] = rng.choice([-7, -1, inp["permutedRows"], 2**31 - 1], size=int(pick.sum()))
+    dup = rng.random(si.size) < 0.1
+    si[dup] = rng.integers(0, 50, size=int(dup.sum()))
+    inp["probs"][rng.random(inp["probs"].shape) < 0.2] = 0.0
+    check(inp)
+    p = w.make_unpermute_padded(T=128, Eu=16, k=4, H=64, dtype=0, probs_dtype=0, mult=7, seed=6)
+    si = p["sortedIndices"]
+    pick = rng.random(si.size) < 0.1
+    si[pick] = rng.choice([-1, 128, 999], size=int(pick.sum()))
+    dup = rng.random(si.size) < 0.15
+    si[dup] = rng.integers(0, 8, size=int(dup.sum()))
+    check(p)
+
+
+def test_topk_512_and_empty_tokens():
+    """topK_num = 512 (the largest allowed), most slots unused."""
+    T, k, H = 12, 512, 32
+    inp = w.make_unpermute_topk(T=T, k=k, Eu=600, H=H, dtype=1, probs_dtype=1, choices=(0, 3, 512),
+                                seed=9)
+    check(inp)
+
+
+def test_more_routing_ones_than_slots():
+    """maskedSelect output longer than n: truncated."""
+    inp = w.make_unpermute_topk(T=40, k=4, Eu=10, H=16, dtype=3, probs_dtype=3, choices=(4,), seed=3)
+    inp["routingMap"][:] = 1
+    inp["probs"] = np.random.default_rng(3).random((40, 10)).astype(np.float32)
+    check(inp)
+
+
+@pytest.mark.parametrize("rows_extra", [0, 5])
+def test_no_probs_restore_shape(rows_extra):
+    """Branches (3)/(4) take the token count from restoreShape."""
+    inp = w.make_unpermute_topk(T=100, k=3, Eu=8, H=24, dtype=3, probs_dtype=None, choices=(1, 3),
+                                seed=4, rows=300 + rows_extra)
+    check(inp)
+
+
+def test_large_sort_two_passes():
+    """More than 4096 distinct keys: the index sort runs as LSD passes."""
+    inp = w.make_unpermute_topk(T=3000, k=4, Eu=32, H=16, dtype=1, probs_dtype=1, choices=(2, 4),
+                                seed=10)
+    check(inp)
+    p = w.make_unpermute_padded(T=8192, Eu=64, k=2, H=16, dtype=0, probs_dtype=3, mult=9, seed=10)
+    check(p)
+
+
+def test_workspace_reuse_and_side_stream():
+    import unpermute_stable_counting_gb300 as usc
+    a = w.make_unpermute_topk(T=200, k=8, Eu=32, H=64, dtype=1, probs_dtype=1, seed=41)
+    b = w.make_unpermute_padded(T=256, Eu=32, k=4, H=64, dtype=0, probs_dtype=3, mult=3, seed=42)
+    s = torch.cuda.Stream()
+    ws = torch.empty(1 << 22, dtype=torch.uint8, device="cuda:0")
+    with torch.cuda.stream(s):
+        ga = unpermute_numpy(run_unpermute(a, workspace=ws, stream=s), a)
+        gb = unpermute_numpy(run_unpermute(b, workspace=ws, stream=s), b)
+        ga2 = unpermute_numpy(run_unpermute(a, workspace=ws, stream=s), a)
+    assert_unpermute_equal(ga, oracle.unpermute(a), a)
+    assert_unpermute_equal(gb, oracle.unpermute(b), b)
+    assert_unpermute_equal(ga2, oracle.unpermute(a), a)

@@ -1,0 +1,61 @@
+"""ctypes declarations of the C ABI in include/moe_reorder.h.
+
+Loading fails loudly when libmoe_reorder.so is missing: there is no CPU or
+PyTorch fallback for any operation of this package.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import _build
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I32 = ctypes.c_int32
+_U64 = ctypes.c_uint64
+_PI64 = ctypes.POINTER(ctypes.c_int64)
+_PU64 = ctypes.POINTER(ctypes.c_uint64)
+
+# name -> (restype, argtypes); every function declared in include/moe_reorder.h
+SIGNATURES = {
+    "ffnwb_batching_get_workspace_size": (_I32, [_I64, _PI64, _I64, _I64, _I64, _PU64]),
+    "ffnwb_batching": (_I32, [_P, _I32, _P, _I64, _P, _I64, _P, _P, _P, _I64, _PI64, _I64, _I64,
+                              _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _U64, _P]),
+    "moe_unpermute_get_workspace_size": (_I32, [_I64, _I64, _I32, _I64, _I32, _I32, _I64, _I64,
+                                                _I32, _PI64, _PU64]),
+    "moe_unpermute": (_I32, [_P, _P, _P, _P, _I64, _I64, _I32, _I64, _I32, _I64, _I64, _I32, _PI64,
+                             _P, _P, _P, _P, _P, _U64, _P]),
+    "mr_status_string": (ctypes.c_char_p, [_I32]),
+    "mr_version": (_I32, []),
+    "mr_profile_set_events": (_I32, [ctypes.POINTER(_P), _I32]),
+}
+
+_lib = None
+
+
+class LibraryMissing(ImportError):
+    pass
+
+
+def lib(path: str | None = None) -> ctypes.CDLL:
+    """The loaded library (loaded once)."""
+    global _lib
+    if _lib is None:
+        p = path or _build.LIB_PATH
+        if not os.path.exists(p):
+            raise LibraryMissing(
+                f"{p} is not built; run unpermute_stable_counting_gb300._build.build_library() "
+                "(or __graft_entry__.build()) first")
+        L = ctypes.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def int64_array(values) -> ctypes.Array:
+    arr = (ctypes.c_int64 * len(values))(*[int(v) for v in values])
+    return arr

@@ -1,0 +1,260 @@
+// FFN-worker batching on GB300.
+//
+// "aclnnFfnWorkerBatching", 功能说明 steps 2-4 and 计算公式:
+//   gather_idx, _ = sort(expert_ids_in)   (masked slots keyed large)
+//   y[i] = token_data[gather_idx[i]]      (+ the fp32 dynamic scale in INT8 mode)
+//   group_list[e] = [expert_id_e, expert_token_num_e]
+//   actual_token_num = sum_e expert_token_num_e
+//
+// Launch sequence on the caller's stream (all PDL-chained):
+//   1. csort rank    : stable in-tile ranks and tile histograms of the keys
+//   2. csort prefix  : per-key tile offsets, key starts, group_list and
+//                      actual_token_num (replaces the page's single-core
+//                      jump-point scan)
+//   3. scatter       : every slot's output row; the four int32 id outputs,
+//                      gather_idx (workspace) and the optional slot -> row map
+//   4. row gather    : y rows (and dynamic scales), one warp per row,
+//                      16-byte streaming loads/stores when aligned
+#include <cstdio>
+#include <cstdlib>
+
+#include "csort.cuh"
+
+namespace mr {
+
+// key(s) = layer_id*E_l + id for 0 <= id < E_l, else the sentinel E.
+struct BatchKey {
+    const int32_t* ids;
+    int32_t layer_base;  // layer_id * E_l
+    int32_t El;
+    int32_t E;
+    __device__ __forceinline__ int operator()(int64_t s) const {
+        const int32_t id = __ldg(ids + s);
+        return (id >= 0 && id < El) ? layer_base + id : E;
+    }
+};
+
+__global__ void __launch_bounds__(256)
+batching_scatter_kernel(BatchKey kf, int64_t Y, int B, CsortBufs cs,
+                        const int32_t* __restrict__ sess_in, const int32_t* __restrict__ micro_in,
+                        const int32_t* __restrict__ tok_in, int32_t* __restrict__ sess_out,
+                        int32_t* __restrict__ micro_out, int32_t* __restrict__ tok_out,
+                        int32_t* __restrict__ eoff_out, int32_t* __restrict__ gather_idx,
+                        int32_t* __restrict__ slot_row) {
+    grid_dependency_wait();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < Y; s += stride) {
+        const int k = kf(s);
+        const uint32_t d = csort_dest(k, s, cs, B);
+        gather_idx[d] = (int32_t)s;
+        if (k < kf.E) {
+            sess_out[d] = sess_in[s];
+            micro_out[d] = micro_in[s];
+            tok_out[d] = tok_in ? tok_in[s] : (int32_t)s;
+            eoff_out[d] = (int32_t)(d - cs.bucket_start[k]);
+            if (slot_row) slot_row[s] = (int32_t)d;
+        } else {
+            sess_out[d] = -1;
+            micro_out[d] = -1;
+            tok_out[d] = -1;
+            eoff_out[d] = -1;
+            if (slot_row) slot_row[s] = -1;
+        }
+    }
+}
+
+// Copy `bytes` from src to dst with one warp. Vector width follows the common
+// alignment of both addresses and the length.
+template <int VPT>
+__device__ __forceinline__ void warp_copy_row(const uint8_t* __restrict__ src,
+                                              uint8_t* __restrict__ dst, int64_t bytes, int lane) {
+    const uintptr_t mis = (reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) |
+                           (uintptr_t)bytes);
+    if ((mis & 15u) == 0u) {
+        const int64_t nv = bytes >> 4;
+        int64_t v = lane;
+        for (; v + 32 * (VPT - 1) < nv; v += 32 * VPT) {
+            uint4 r[VPT];
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) r[u] = ld_stream_v4(src + 16 * (v + 32 * u));
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) st_stream_v4(dst + 16 * (v + 32 * u), r[u]);
+        }
+        uint4 r[VPT];
+#pragma unroll
+        for (int u = 0; u < VPT; ++u)
+            if (v + 32 * u < nv) r[u] = ld_stream_v4(src + 16 * (v + 32 * u));
+#pragma unroll
+        for (int u = 0; u < VPT; ++u)
+            if (v + 32 * u < nv) st_stream_v4(dst + 16 * (v + 32 * u), r[u]);
+    } else if ((mis & 3u) == 0u) {
+        constexpr int W = VPT * 4;
+        const int64_t nw = bytes >> 2;
+        int64_t v = lane;
+        for (; v + 32 * (W - 1) < nw; v += 32 * W) {
+            uint32_t r[W];
+#pragma unroll
+            for (int u = 0; u < W; ++u) r[u] = ld_stream_u32(src + 4 * (v + 32 * u));
+#pragma unroll
+            for (int u = 0; u < W; ++u) st_stream_u32(dst + 4 * (v + 32 * u), r[u]);
+        }
+        for (; v < nw; v += 32) st_stream_u32(dst + 4 * v, ld_stream_u32(src + 4 * v));
+    } else {
+        for (int64_t b = lane; b < bytes; b += 32) dst[b] = src[b];
+    }
+}
+
+template <int VPT>
+__global__ void __launch_bounds__(256)
+batching_gather_kernel(const uint8_t* __restrict__ token_data, int64_t row_stride,
+                       int64_t row_bytes, int is_int8, const uint8_t* __restrict__ scales,
+                       int64_t scale_stride, uint8_t* __restrict__ y, float* __restrict__ dyn,
+                       const int32_t* __restrict__ gather_idx,
+                       const uint32_t* __restrict__ bucket_start, int E) {
+    grid_dependency_wait();
+    const uint32_t U = bucket_start[E];
+    const int lane = threadIdx.x & 31;
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t i = gw; i < (int64_t)U; i += nw) {
+        const int64_t g = gather_idx[i];
+        warp_copy_row<VPT>(token_data + g * row_stride, y + i * row_bytes, row_bytes, lane);
+        if (is_int8 && lane < 4) {
+            // 4 scale bytes, one per lane (the scale is only 4-byte aligned at best)
+            const uint8_t* sp = scales ? scales + g * scale_stride : token_data + g * row_stride + row_bytes;
+            reinterpret_cast<uint8_t*>(dyn + i)[lane] = sp[lane];
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+struct BatchPlan {
+    int64_t A, BS, K1, H, Y, E, L, El;
+    int dtype;
+    int B;
+    int64_t row_bytes;
+    uint64_t ws_bytes;
+};
+
+static mr_status plan_batching(int64_t expertNum, const int64_t* maxOutShape, int64_t tokenDtype,
+                               int64_t needSchedule, int64_t layerNum, BatchPlan* p) {
+    if (!maxOutShape) return MR_ERR_PARAM_NULLPTR;
+    const int64_t A = maxOutShape[0], BS = maxOutShape[1], K1 = maxOutShape[2], H = maxOutShape[3];
+    if (expertNum <= 0 || expertNum > MR_MAX_EXPERT_NUM) return MR_ERR_PARAM_INVALID;
+    if (A <= 0 || A > MR_MAX_A || BS <= 0 || K1 <= 0 || K1 > MR_MAX_TOPK1 || H <= 0)
+        return MR_ERR_PARAM_INVALID;
+    if (tokenDtype != MR_DTYPE_F16 && tokenDtype != MR_DTYPE_BF16 && tokenDtype != MR_DTYPE_INT8)
+        return MR_ERR_PARAM_INVALID;
+    if (needSchedule != 0 && needSchedule != 1) return MR_ERR_PARAM_INVALID;
+    if (layerNum < 0 || layerNum > expertNum) return MR_ERR_PARAM_INVALID;
+    const int64_t L = layerNum > 0 ? layerNum : 1;
+    if (expertNum % L != 0) return MR_ERR_PARAM_INVALID;
+    if (BS > (INT64_C(1) << 31) || A * BS > (INT64_C(1) << 31) || A * BS * K1 >= (INT64_C(1) << 31))
+        return MR_ERR_PARAM_INVALID;
+    if (H > (INT64_C(1) << 40)) return MR_ERR_PARAM_INVALID;
+    if (needSchedule == 1) return MR_ERR_UNSUPPORTED;
+    p->A = A;
+    p->BS = BS;
+    p->K1 = K1;
+    p->H = H;
+    p->Y = A * BS * K1;
+    p->E = expertNum;
+    p->L = L;
+    p->El = expertNum / L;
+    p->dtype = (int)tokenDtype;
+    p->B = (int)expertNum + 1;
+    p->row_bytes = H * (tokenDtype == MR_DTYPE_INT8 ? 1 : 2);
+    p->ws_bytes = csort_workspace_bytes(p->Y, p->B) + align_up((uint64_t)p->Y * 4u, 256);
+    return MR_OK;
+}
+
+static int gather_grid(int64_t rows) {
+    static int blocks_per_sm[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int bps = dev < 64 ? blocks_per_sm[dev] : 0;
+    if (bps == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, batching_gather_kernel<7>, 256, 0) !=
+                cudaSuccess || bps <= 0)
+            bps = 4;
+        if (dev < 64) blocks_per_sm[dev] = bps;
+    }
+    const int64_t want = (rows + 7) / 8;  // 8 warps per block, one row per warp
+    const int64_t cap = (int64_t)device_sm_count() * bps;
+    int64_t g = want < cap ? want : cap;
+    return (int)(g > 0 ? g : 1);
+}
+
+}  // namespace mr
+
+using namespace mr;
+
+extern "C" mr_status ffnwb_batching_get_workspace_size(int64_t expertNum, const int64_t* maxOutShape,
+                                                        int64_t tokenDtype, int64_t needSchedule,
+                                                        int64_t layerNum, uint64_t* workspaceSize) {
+    if (!workspaceSize) return MR_ERR_PARAM_NULLPTR;
+    BatchPlan p;
+    const mr_status st = plan_batching(expertNum, maxOutShape, tokenDtype, needSchedule, layerNum, &p);
+    if (st != MR_OK) return st;
+    *workspaceSize = p.ws_bytes;
+    return MR_OK;
+}
+
+extern "C" mr_status ffnwb_batching(const int32_t* expertIds, int32_t layerId, const void* tokenData,
+                                    int64_t tokenRowStride, const void* scales, int64_t scaleStride,
+                                    const int32_t* sessionIdsIn, const int32_t* microBatchIdsIn,
+                                    const int32_t* tokenIdsIn, int64_t expertNum,
+                                    const int64_t* maxOutShape, int64_t tokenDtype,
+                                    int64_t needSchedule, int64_t layerNum, void* y,
+                                    int64_t* groupList, int32_t* sessionIds, int32_t* microBatchIds,
+                                    int32_t* tokenIds, int32_t* expertOffsets, float* dynamicScale,
+                                    int64_t* actualTokenNum, int32_t* sortedIndicesOut,
+                                    void* workspace, uint64_t workspaceSize, void* stream) {
+    BatchPlan p;
+    mr_status st = plan_batching(expertNum, maxOutShape, tokenDtype, needSchedule, layerNum, &p);
+    if (st != MR_OK) return st;
+    if (!expertIds || !tokenData || !sessionIdsIn || !microBatchIdsIn || !y || !groupList ||
+        !sessionIds || !microBatchIds || !tokenIds || !expertOffsets || !actualTokenNum)
+        return MR_ERR_PARAM_NULLPTR;
+    const bool int8 = p.dtype == MR_DTYPE_INT8;
+    if (int8 && !dynamicScale) return MR_ERR_PARAM_NULLPTR;
+    if (!workspace && p.ws_bytes > 0) return MR_ERR_PARAM_NULLPTR;
+    if (layerId < 0 || layerId >= p.L) return MR_ERR_PARAM_INVALID;
+    const int64_t need_stride = p.row_bytes + ((int8 && !scales) ? 4 : 0);
+    if (tokenRowStride < need_stride) return MR_ERR_PARAM_INVALID;
+    if (int8 && scales && scaleStride < 4) return MR_ERR_PARAM_INVALID;
+    if (workspaceSize < p.ws_bytes) return MR_ERR_WORKSPACE;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* wp = reinterpret_cast<uint8_t*>(workspace);
+    CsortBufs cs = csort_carve(wp, p.Y, p.B);
+    int32_t* gather_idx = reinterpret_cast<int32_t*>(wp);
+
+    BatchKey kf{expertIds, (int32_t)(layerId * p.El), (int32_t)p.El, (int32_t)p.E};
+    GroupListOut gl{groupList, actualTokenNum, (int)p.E};
+
+    profile_mark(s, 0);
+    MR_TRY_CUDA(csort_run(kf, p.Y, p.B, cs, gl, s));
+    {
+        const int64_t want = (p.Y + 255) / 256;
+        const int64_t cap = (int64_t)device_sm_count() * 8;
+        const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
+        MR_TRY_CUDA(launch_pdl(batching_scatter_kernel, dim3(grid), dim3(256), 0, s, kf, p.Y, p.B,
+                               cs, sessionIdsIn, microBatchIdsIn, tokenIdsIn, sessionIds,
+                               microBatchIds, tokenIds, expertOffsets, gather_idx,
+                               sortedIndicesOut));
+    }
+    profile_mark(s, 1);
+    profile_mark(s, 2);
+    MR_TRY_CUDA(launch_pdl(batching_gather_kernel<7>, dim3(gather_grid(p.Y)), dim3(256), 0, s,
+                           reinterpret_cast<const uint8_t*>(tokenData), tokenRowStride,
+                           p.row_bytes, int8 ? 1 : 0, reinterpret_cast<const uint8_t*>(scales),
+                           scaleStride, reinterpret_cast<uint8_t*>(y), dynamicScale, gather_idx,
+                           cs.bucket_start, (int)p.E));
+    profile_mark(s, 3);
+    MR_TRY_CUDA(cudaGetLastError());
+    return MR_OK;
+}

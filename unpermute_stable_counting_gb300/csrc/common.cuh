@@ -1,0 +1,152 @@
+// Shared device/host helpers of the GB300 reorder library (sm_103a).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_fp16.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/moe_reorder.h"
+
+namespace mr {
+
+constexpr int kNumSMsHint = 152;  // GB300; the launch code queries the real count
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch. Every kernel of the library calls
+// grid_dependency_wait() before its first global-memory access, so a kernel
+// launched early (programmatic stream serialisation) never reads or writes
+// memory that the previous kernel in the stream still uses.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void allow_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// Cache-hinted global accesses for streamed data (read once / written once).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_stream_v4(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+__device__ __forceinline__ uint32_t ld_stream_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.L1::no_allocate.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+__device__ __forceinline__ void st_stream_u32(void* p, uint32_t v) {
+    asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// ---------------------------------------------------------------------------
+// Block-wide exclusive scan of one uint32 per thread (blockDim.x multiple of
+// 32, at most 1024). `warp_sums` must hold 32 entries. Returns the exclusive
+// prefix; *total receives the block sum.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t block_exclusive_scan(uint32_t v, uint32_t* warp_sums,
+                                                         uint32_t* total) {
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int nwarps = blockDim.x >> 5;
+    uint32_t x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        uint32_t y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t s = lane < nwarps ? warp_sums[lane] : 0u;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            uint32_t y = __shfl_up_sync(0xffffffffu, s, o);
+            if (lane >= o) s += y;
+        }
+        warp_sums[lane] = s;  // inclusive prefix of warp sums
+    }
+    __syncthreads();
+    const uint32_t warp_base = warp > 0 ? warp_sums[warp - 1] : 0u;
+    if (total) *total = warp_sums[nwarps - 1];
+    const uint32_t r = warp_base + x - v;
+    __syncthreads();  // warp_sums may be reused by the caller
+    return r;
+}
+
+// ---------------------------------------------------------------------------
+// Element conversions (CUDA intrinsics: exact widening, RNE narrowing).
+// ---------------------------------------------------------------------------
+template <int DT> struct Elem;
+template <> struct Elem<MR_DTYPE_F16> {
+    using T = __half;
+    static __device__ __forceinline__ float to_f32(uint16_t b) {
+        return __half2float(__ushort_as_half(b));
+    }
+    static __device__ __forceinline__ uint16_t from_f32(float f) {
+        return __half_as_ushort(__float2half_rn(f));
+    }
+};
+template <> struct Elem<MR_DTYPE_BF16> {
+    static __device__ __forceinline__ float to_f32(uint16_t b) {
+        return __bfloat162float(__ushort_as_bfloat16(b));
+    }
+    static __device__ __forceinline__ uint16_t from_f32(float f) {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+    }
+};
+
+__device__ __forceinline__ float load_f32(const void* base, int64_t i, int dt) {
+    if (dt == MR_DTYPE_F32) return reinterpret_cast<const float*>(base)[i];
+    const uint16_t b = reinterpret_cast<const uint16_t*>(base)[i];
+    return dt == MR_DTYPE_F16 ? Elem<MR_DTYPE_F16>::to_f32(b) : Elem<MR_DTYPE_BF16>::to_f32(b);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+inline uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+
+int device_sm_count();                 // cached per device
+void profile_mark(cudaStream_t s, int event_index);  // records a timing event if set
+
+// Launch with programmatic stream serialisation (PDL) enabled.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
+}  // namespace mr
+
+#define MR_TRY_CUDA(expr)                                   \
+    do {                                                    \
+        cudaError_t _e = (expr);                            \
+        if (_e != cudaSuccess) return MR_ERR_CUDA;          \
+    } while (0)

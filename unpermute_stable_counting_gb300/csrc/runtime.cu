@@ -1,0 +1,50 @@
+// Host utilities of the reorder library: device queries, status text and the
+// per-thread timing hooks used by benchmarks.
+#include "common.cuh"
+
+namespace mr {
+
+namespace {
+int g_sm_count[64] = {0};
+thread_local cudaEvent_t g_events[16] = {nullptr};
+thread_local int g_num_events = 0;
+}  // namespace
+
+int device_sm_count() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return kNumSMsHint;
+    if (dev >= 0 && dev < 64 && g_sm_count[dev] > 0) return g_sm_count[dev];
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = kNumSMsHint;
+    if (dev >= 0 && dev < 64) g_sm_count[dev] = n;
+    return n;
+}
+
+void profile_mark(cudaStream_t s, int event_index) {
+    if (event_index < g_num_events && g_events[event_index]) cudaEventRecord(g_events[event_index], s);
+}
+
+}  // namespace mr
+
+extern "C" const char* mr_status_string(mr_status status) {
+    switch (status) {
+        case MR_OK: return "ok";
+        case MR_ERR_PARAM_NULLPTR: return "a required pointer is NULL";
+        case MR_ERR_PARAM_INVALID: return "a dtype, shape or range is outside the supported set";
+        case MR_ERR_INNER: return "topK_num > 512 or a probs shape outside the supported range";
+        case MR_ERR_CUDA: return "the CUDA runtime reported an error";
+        case MR_ERR_WORKSPACE: return "workspaceSize is smaller than required";
+        case MR_ERR_UNSUPPORTED: return "a valid mode that this library does not implement";
+    }
+    return "unknown status";
+}
+
+extern "C" int32_t mr_version(void) { return 100; }
+
+extern "C" mr_status mr_profile_set_events(void* const* events, int32_t count) {
+    if (count < 0 || count > 16 || (count > 0 && !events)) return MR_ERR_PARAM_INVALID;
+    for (int i = 0; i < 16; ++i) mr::g_events[i] = i < count ? reinterpret_cast<cudaEvent_t>(events[i]) : nullptr;
+    mr::g_num_events = count;
+    return MR_OK;
+}

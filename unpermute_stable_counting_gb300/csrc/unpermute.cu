@@ -1,0 +1,717 @@
+// Routing-map unpermute on GB300.
+//
+// "MoeTokenUnpermuteWithRoutingMap 算子全解析", 功能说明与计算公式 (branches
+// (1)-(4)) and Kernel 实现 (pad-kernel prob lookup, IsValidInputIndex, the
+// prob != 0 skip, fp32 Cast/Muls/Add and the CAST_RINT back-cast).
+//
+// Launch sequence on the caller's stream (PDL-chained):
+//   not padded, probs : maskedSelect = column bitmasks -> csort prefix ->
+//                       scatter (+ zero tail)
+//   padded, probs     : permuteProbs[i] = probs[sortedIndices[i], i // capacity]
+//   always            : stable sort of sortedIndices (1-3 LSD passes of the
+//                       counting-sort engine) -> outIndex, permuteTokenId;
+//                       padded: per-token row ranges (CSR) from the sorted keys
+//   always            : gather-reduce, one CTA per (token, hidden slice),
+//                       fp32 accumulation in ascending slot / row order,
+//                       atomic-free, one RNE cast per output element.
+#include <cstdio>
+#include <cstdlib>
+
+#include "csort.cuh"
+
+namespace mr {
+
+template <int DT>
+__device__ __forceinline__ float ld_f32(const void* base, int64_t i) {
+    if constexpr (DT == MR_DTYPE_F32) {
+        return __ldg(reinterpret_cast<const float*>(base) + i);
+    } else {
+        const uint16_t b = __ldg(reinterpret_cast<const unsigned short*>(base) + i);
+        return Elem<DT>::to_f32(b);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// maskedSelect of probs.T by routingMap.T (not padded, with probs).
+// The routing map is cut into blocks of 32 tokens; item (blk, e) holds the
+// 32-bit mask of the block's tokens routed to expert e. Its popcount is the
+// histogram entry of the counting sort whose key is the expert, so the
+// engine's prefix kernel turns them into positions: the j-th token of the
+// mask lands at bucket_start[e] + tile_off[blk][e] + (set bits below j).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+mask_columns_kernel(const int8_t* __restrict__ map, int64_t T, int64_t Eu,
+                    uint32_t* __restrict__ masks, uint32_t* __restrict__ counts,
+                    uint32_t* __restrict__ ticket) {
+    grid_dependency_wait();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
+    const int64_t nblk = (T + 31) / 32;
+    const int64_t items = nblk * Eu;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < items; it += stride) {
+        const int64_t blk = it / Eu;
+        const int64_t e = it - blk * Eu;
+        const int64_t t0 = blk * 32;
+        const int nt = (int)(T - t0 < 32 ? T - t0 : 32);
+        uint32_t bits = 0u;
+        for (int j = 0; j < nt; ++j) bits |= (map[(t0 + j) * Eu + e] != 0 ? 1u : 0u) << j;
+        masks[it] = bits;
+        counts[it] = __popc(bits);
+    }
+}
+
+__global__ void __launch_bounds__(256)
+mask_scatter_kernel(const uint32_t* __restrict__ masks, const uint32_t* __restrict__ offs,
+                    const uint32_t* __restrict__ bucket_start, int64_t T, int64_t Eu, int64_t n,
+                    const uint8_t* __restrict__ probs, int pes, uint8_t* __restrict__ pp) {
+    grid_dependency_wait();
+    const int64_t nblk = (T + 31) / 32;
+    const int64_t items = nblk * Eu;
+    const int64_t nnz = bucket_start[Eu];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t total = items > n ? items : n;
+    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total; it += stride) {
+        if (it < items) {
+            uint32_t bits = masks[it];
+            if (bits) {
+                const int64_t blk = it / Eu;
+                const int64_t e = it - blk * Eu;
+                int64_t pos = (int64_t)bucket_start[e] + offs[it];
+                while (bits && pos < n) {
+                    const int j = __ffs(bits) - 1;
+                    bits &= bits - 1u;
+                    const int64_t src = ((blk * 32 + j) * Eu + e) * pes;
+                    for (int b = 0; b < pes; ++b) pp[pos * pes + b] = probs[src + b];
+                    ++pos;
+                }
+            }
+        }
+        if (it >= nnz && it < n) {
+            for (int b = 0; b < pes; ++b) pp[it * pes + b] = 0;
+        }
+    }
+}
+
+// permuteProbs[i] = probs[sortedIndices[i], i // capacity]  (padded, with probs)
+__global__ void __launch_bounds__(256)
+padded_probs_kernel(const int32_t* __restrict__ si, int64_t n, int64_t T, int64_t Eu, int64_t cap,
+                    const uint8_t* __restrict__ probs, int pes, uint8_t* __restrict__ pp) {
+    grid_dependency_wait();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const int32_t v = si[i];
+        if (v >= 0 && v < T) {
+            const int64_t src = ((int64_t)v * Eu + i / cap) * pes;
+            for (int b = 0; b < pes; ++b) pp[i * pes + b] = probs[src + b];
+        } else {
+            for (int b = 0; b < pes; ++b) pp[i * pes + b] = 0;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Stable sort of sortedIndices (LSD passes of the counting-sort engine).
+// Full key: not padded (invalid first) v+1 for 0 <= v < rows, else 0;
+//           padded (invalid last)      v   for 0 <= v < T,    else T.
+// ---------------------------------------------------------------------------
+struct RadixKey {
+    const int32_t* si;        // pass 0 source
+    const uint32_t* keys_in;  // later passes: full keys in the previous order
+    int64_t limit;            // rows (not padded) or T (padded)
+    int padded;
+    int shift;
+    uint32_t mask;
+    __device__ __forceinline__ uint32_t full(int64_t i) const {
+        if (keys_in) return keys_in[i];
+        const int32_t v = si[i];
+        const bool ok = v >= 0 && (int64_t)v < limit;
+        if (padded) return ok ? (uint32_t)v : (uint32_t)limit;
+        return ok ? (uint32_t)v + 1u : 0u;
+    }
+    __device__ __forceinline__ int operator()(int64_t i) const {
+        return (int)((full(i) >> shift) & mask);
+    }
+};
+
+__global__ void __launch_bounds__(256)
+radix_scatter_kernel(RadixKey kf, int64_t n, int B, CsortBufs cs, const int32_t* __restrict__ idx_in,
+                     uint32_t* __restrict__ keys_out, int32_t* __restrict__ idx_out,
+                     int32_t* __restrict__ out_index, int32_t* __restrict__ ptid, int64_t topk) {
+    grid_dependency_wait();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const uint32_t fk = kf.full(i);
+        const int digit = (int)((fk >> kf.shift) & kf.mask);
+        const uint32_t d = csort_dest(digit, i, cs, B);
+        const int32_t idx = idx_in ? idx_in[i] : (int32_t)i;
+        keys_out[d] = fk;
+        if (out_index) {
+            out_index[d] = idx;
+            ptid[d] = kf.padded ? kf.si[idx] : (int32_t)(idx / topk);
+        } else {
+            idx_out[d] = idx;
+        }
+    }
+}
+
+// ptr[t] = first position of the sorted keys with key >= t, t in [0, T].
+__global__ void __launch_bounds__(256)
+csr_from_keys_kernel(const uint32_t* __restrict__ keys, int64_t n, int64_t T,
+                     int32_t* __restrict__ ptr) {
+    grid_dependency_wait();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p <= n; p += stride) {
+        const int64_t prev = p > 0 ? (int64_t)keys[p - 1] : -1;
+        const int64_t cur = p < n ? (int64_t)keys[p] : T + 1;
+        const int64_t hi = cur < T ? cur : T;
+        for (int64_t t = prev + 1; t <= hi; ++t) ptr[t] = (int32_t)p;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Gather-reduce. One CTA per (token, hidden slice). Warp 0 builds the
+// token's list of contributing rows in ascending order (valid index and,
+// with probs, nonzero prob) in shared memory; every thread then owns up to
+// kRedQ 16-byte output vectors and adds the rows in list order in fp32:
+// acc = acc + f32(x) * f32(p), each operation rounded on its own.
+// ---------------------------------------------------------------------------
+constexpr int kListCap = 512;
+constexpr int kRedUnroll = 4;
+constexpr int kRedQ = 2;
+
+template <bool HAS_PROBS, bool PADDED, int PDT>
+__device__ __forceinline__ int build_list(int64_t c0, int64_t c1, const int32_t* __restrict__ si,
+                                          int64_t rows, int64_t row_bytes,
+                                          const void* __restrict__ pp,
+                                          const int32_t* __restrict__ out_index, int64_t* s_row,
+                                          float* s_w) {
+    const int lane = threadIdx.x & 31;
+    int cnt = 0;
+    for (int64_t e0 = c0; e0 < c1; e0 += 32) {
+        const int64_t e = e0 + lane;
+        bool keep = false;
+        int64_t r = 0;
+        float w = 1.0f;
+        if (e < c1) {
+            if (PADDED) {
+                r = out_index[e];
+                keep = true;
+            } else {
+                const int32_t v = si[e];
+                keep = v >= 0 && (int64_t)v < rows;
+                r = v;
+            }
+            if (HAS_PROBS && keep) {
+                w = ld_f32<PDT>(pp, PADDED ? r : e);
+                keep = w != 0.0f;
+            }
+        }
+        const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+        if (keep) {
+            const int pos = cnt + __popc(bal & lanemask_lt());
+            s_row[pos] = r * row_bytes;
+            s_w[pos] = w;
+        }
+        cnt += __popc(bal);
+    }
+    return cnt;
+}
+
+template <int TDT>
+struct Vec;
+template <>
+struct Vec<MR_DTYPE_F32> {
+    static constexpr int N = 4;
+    static __device__ __forceinline__ void unpack(const uint4& v, float* x) {
+        x[0] = __uint_as_float(v.x);
+        x[1] = __uint_as_float(v.y);
+        x[2] = __uint_as_float(v.z);
+        x[3] = __uint_as_float(v.w);
+    }
+    static __device__ __forceinline__ uint4 pack(const float* a) {
+        return make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
+                          __float_as_uint(a[3]));
+    }
+};
+template <int DT>
+struct Vec16 {
+    static constexpr int N = 8;
+    static __device__ __forceinline__ void unpack(const uint4& v, float* x) {
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x[2 * k] = Elem<DT>::to_f32((uint16_t)(w[k] & 0xffffu));
+            x[2 * k + 1] = Elem<DT>::to_f32((uint16_t)(w[k] >> 16));
+        }
+    }
+    static __device__ __forceinline__ uint4 pack(const float* a) {
+        uint32_t w[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            w[k] = (uint32_t)Elem<DT>::from_f32(a[2 * k]) |
+                   ((uint32_t)Elem<DT>::from_f32(a[2 * k + 1]) << 16);
+        return make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+template <>
+struct Vec<MR_DTYPE_F16> : Vec16<MR_DTYPE_F16> {};
+template <>
+struct Vec<MR_DTYPE_BF16> : Vec16<MR_DTYPE_BF16> {};
+
+template <int TDT, int PDT, bool HAS_PROBS, bool PADDED>
+__global__ void __launch_bounds__(1024)
+unpermute_reduce_vec_kernel(const uint8_t* __restrict__ permuted, int64_t rows, int64_t row_bytes,
+                            int64_t nvec, int64_t slice_vec, const int32_t* __restrict__ si,
+                            int64_t topk, const void* __restrict__ pp,
+                            const int32_t* __restrict__ out_index, const int32_t* __restrict__ ptr,
+                            int64_t T, uint8_t* __restrict__ out) {
+    using V = Vec<TDT>;
+    __shared__ int64_t s_row[kListCap];
+    __shared__ float s_w[kListCap];
+    __shared__ int s_cnt;
+    grid_dependency_wait();
+    const int64_t v0 = (int64_t)blockIdx.y * slice_vec;
+    const int64_t v1 = v0 + slice_vec < nvec ? v0 + slice_vec : nvec;
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        int64_t L0, L1;
+        if (PADDED) {
+            L0 = ptr[t];
+            L1 = ptr[t + 1];
+        } else {
+            L0 = t * topk;
+            L1 = L0 + topk;
+        }
+        float acc[kRedQ][V::N];
+#pragma unroll
+        for (int q = 0; q < kRedQ; ++q)
+#pragma unroll
+            for (int k = 0; k < V::N; ++k) acc[q][k] = 0.0f;
+
+        for (int64_t c0 = L0; c0 < L1; c0 += kListCap) {
+            const int64_t c1 = c0 + kListCap < L1 ? c0 + kListCap : L1;
+            if (threadIdx.x < 32) {
+                const int cnt = build_list<HAS_PROBS, PADDED, PDT>(c0, c1, si, rows, row_bytes, pp,
+                                                                   out_index, s_row, s_w);
+                if (threadIdx.x == 0) s_cnt = cnt;
+            }
+            __syncthreads();
+            const int cnt = s_cnt;
+            for (int m0 = 0; m0 < cnt; m0 += kRedUnroll) {
+                uint4 x[kRedUnroll][kRedQ];
+#pragma unroll
+                for (int u = 0; u < kRedUnroll; ++u) {
+                    if (m0 + u < cnt) {
+                        const uint8_t* rp = permuted + s_row[m0 + u];
+#pragma unroll
+                        for (int q = 0; q < kRedQ; ++q) {
+                            const int64_t v = v0 + threadIdx.x + (int64_t)q * blockDim.x;
+                            if (v < v1) x[u][q] = ld_stream_v4(rp + 16 * v);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kRedUnroll; ++u) {
+                    if (m0 + u < cnt) {
+                        const float w = s_w[m0 + u];
+#pragma unroll
+                        for (int q = 0; q < kRedQ; ++q) {
+                            const int64_t v = v0 + threadIdx.x + (int64_t)q * blockDim.x;
+                            if (v < v1) {
+                                float xs[V::N];
+                                V::unpack(x[u][q], xs);
+#pragma unroll
+                                for (int k = 0; k < V::N; ++k)
+                                    acc[q][k] = HAS_PROBS ? __fadd_rn(acc[q][k], __fmul_rn(xs[k], w))
+                                                          : __fadd_rn(acc[q][k], xs[k]);
+                            }
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+        }
+#pragma unroll
+        for (int q = 0; q < kRedQ; ++q) {
+            const int64_t v = v0 + threadIdx.x + (int64_t)q * blockDim.x;
+            if (v < v1) st_stream_v4(out + t * row_bytes + 16 * v, V::pack(acc[q]));
+        }
+    }
+}
+
+// Element-wise variant for rows that are not 16-byte vectors (odd H or
+// buffers not 16-byte aligned; element alignment is required). Same list,
+// same order, same arithmetic.
+template <int TDT, int PDT, bool HAS_PROBS, bool PADDED>
+__global__ void __launch_bounds__(256)
+unpermute_reduce_scalar_kernel(const uint8_t* __restrict__ permuted, int64_t rows, int64_t H,
+                               const int32_t* __restrict__ si, int64_t topk,
+                               const void* __restrict__ pp, const int32_t* __restrict__ out_index,
+                               const int32_t* __restrict__ ptr, int64_t T,
+                               uint8_t* __restrict__ out) {
+    __shared__ int64_t s_row[kListCap];
+    __shared__ float s_w[kListCap];
+    __shared__ int s_cnt;
+    constexpr int es = TDT == MR_DTYPE_F32 ? 4 : 2;
+    grid_dependency_wait();
+    const int64_t row_bytes = H * es;
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        int64_t L0, L1;
+        if (PADDED) {
+            L0 = ptr[t];
+            L1 = ptr[t + 1];
+        } else {
+            L0 = t * topk;
+            L1 = L0 + topk;
+        }
+        for (int64_t h0 = 0; h0 < H; h0 += blockDim.x) {
+            const int64_t h = h0 + threadIdx.x;
+            float acc = 0.0f;
+            for (int64_t c0 = L0; c0 < L1; c0 += kListCap) {
+                const int64_t c1 = c0 + kListCap < L1 ? c0 + kListCap : L1;
+                if (threadIdx.x < 32) {
+                    const int cnt = build_list<HAS_PROBS, PADDED, PDT>(c0, c1, si, rows, row_bytes,
+                                                                       pp, out_index, s_row, s_w);
+                    if (threadIdx.x == 0) s_cnt = cnt;
+                }
+                __syncthreads();
+                const int cnt = s_cnt;
+                if (h < H) {
+                    for (int m = 0; m < cnt; ++m) {
+                        const uint8_t* rp = permuted + s_row[m] + h * es;
+                        float x;
+                        if constexpr (TDT == MR_DTYPE_F32) {
+                            x = __ldg(reinterpret_cast<const float*>(rp));
+                        } else {
+                            x = Elem<TDT>::to_f32(__ldg(reinterpret_cast<const unsigned short*>(rp)));
+                        }
+                        acc = HAS_PROBS ? __fadd_rn(acc, __fmul_rn(x, s_w[m])) : __fadd_rn(acc, x);
+                    }
+                }
+                __syncthreads();
+            }
+            if (h < H) {
+                uint8_t* op = out + t * row_bytes + h * es;
+                if constexpr (TDT == MR_DTYPE_F32) {
+                    *reinterpret_cast<float*>(op) = acc;
+                } else {
+                    *reinterpret_cast<uint16_t*>(op) = Elem<TDT>::from_f32(acc);
+                }
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+constexpr int kRadixDigitBits = 12;
+
+struct UnpermutePlan {
+    int64_t rows, H, n, T, Eu, topk, cap;
+    int tdt, pdt, pes, es;
+    bool probs, padded;
+    // sort
+    uint32_t key_range;  // number of distinct full keys
+    int passes;
+    int shift[3];
+    int bits[3];
+    int Bmax;
+    // workspace
+    uint64_t ms_bytes, sort_bytes, ws_bytes;
+};
+
+static int bits_for(uint64_t range) {  // bits to represent values 0..range-1
+    int b = 0;
+    while (b < 63 && (UINT64_C(1) << b) < range) ++b;
+    return b;
+}
+
+static mr_status plan_unpermute(int64_t permutedRows, int64_t hidden, int32_t tokenDtype,
+                                int64_t n, int32_t hasProbs, int32_t probsDtype, int64_t numTokens,
+                                int64_t numExperts, int32_t paddedMode,
+                                const int64_t* restoreShape, UnpermutePlan* p) {
+    if (tokenDtype != MR_DTYPE_F16 && tokenDtype != MR_DTYPE_BF16 && tokenDtype != MR_DTYPE_F32)
+        return MR_ERR_PARAM_INVALID;
+    if (hasProbs && probsDtype != tokenDtype && probsDtype != MR_DTYPE_F32)
+        return MR_ERR_PARAM_INVALID;
+    if (paddedMode != 0 && paddedMode != 1) return MR_ERR_PARAM_INVALID;
+    if (hidden <= 0 || permutedRows < 0 || n < 0) return MR_ERR_PARAM_INVALID;
+    if (permutedRows >= (INT64_C(1) << 31) || n >= (INT64_C(1) << 31)) return MR_ERR_PARAM_INVALID;
+    int64_t T;
+    if (hasProbs) {
+        if (numTokens <= 0 || numExperts <= 0) return MR_ERR_INNER;
+        T = numTokens;
+        if (restoreShape && (restoreShape[0] != T || restoreShape[1] != hidden))
+            return MR_ERR_PARAM_INVALID;
+    } else {
+        if (!restoreShape) return MR_ERR_PARAM_NULLPTR;
+        T = restoreShape[0];
+        if (T <= 0 || restoreShape[1] != hidden) return MR_ERR_PARAM_INVALID;
+    }
+    if (T >= (INT64_C(1) << 31) - 1) return MR_ERR_PARAM_INVALID;
+    const int64_t topk = permutedRows / T;
+    if (topk > MR_MAX_TOPK_NUM) return MR_ERR_INNER;
+    int64_t cap = 0;
+    if (!paddedMode) {
+        if (n != T * topk) return MR_ERR_PARAM_INVALID;
+    } else {
+        if (n != permutedRows) return MR_ERR_PARAM_INVALID;
+        if (hasProbs) {
+            if (numExperts > n || n % numExperts != 0) return MR_ERR_INNER;
+            cap = n / numExperts;
+        }
+    }
+    if (hasProbs && numExperts > (int64_t)kMaxBuckets - 1) return MR_ERR_INNER;
+    if (hasProbs && T * numExperts >= (INT64_C(1) << 40)) return MR_ERR_INNER;
+    if (paddedMode && hasProbs && getenv("MR_VERBOSE")) {
+        if (topk > numExperts)
+            fprintf(stderr, "moe_unpermute warning: paddedMode with topK_num %lld > experts %lld\n",
+                    (long long)topk, (long long)numExperts);
+        if (cap > T)
+            fprintf(stderr, "moe_unpermute warning: paddedMode with capacity %lld > tokens %lld\n",
+                    (long long)cap, (long long)T);
+    }
+    p->rows = permutedRows;
+    p->H = hidden;
+    p->n = n;
+    p->T = T;
+    p->Eu = hasProbs ? numExperts : 0;
+    p->topk = topk;
+    p->cap = cap;
+    p->tdt = tokenDtype;
+    p->pdt = hasProbs ? probsDtype : tokenDtype;
+    p->pes = p->pdt == MR_DTYPE_F32 ? 4 : 2;
+    p->es = tokenDtype == MR_DTYPE_F32 ? 4 : 2;
+    p->probs = hasProbs != 0;
+    p->padded = paddedMode != 0;
+
+    // sort passes
+    const uint64_t range = paddedMode ? (uint64_t)T + 1 : (uint64_t)permutedRows + 1;
+    p->key_range = (uint32_t)range;
+    if (range <= (UINT64_C(1) << kRadixDigitBits)) {
+        p->passes = 1;
+        p->shift[0] = 0;
+        p->bits[0] = bits_for(range);
+        p->Bmax = (int)range;
+    } else {
+        const int b = bits_for(range);
+        const int P = (b + kRadixDigitBits - 1) / kRadixDigitBits;
+        p->passes = P;
+        int sh = 0;
+        for (int q = 0; q < P; ++q) {
+            const int d = b / P + (q < b % P ? 1 : 0);
+            p->shift[q] = sh;
+            p->bits[q] = d;
+            sh += d;
+        }
+        p->Bmax = 1 << p->bits[0];
+    }
+
+    // workspace
+    uint64_t ms = 0;
+    if (hasProbs && !paddedMode) {
+        const int64_t nblk = (T + 31) / 32;
+        const uint64_t items = (uint64_t)nblk * numExperts;
+        ms = align_up(items * 4u, 256) * 2 + align_up((uint64_t)numExperts * 4u, 256) +
+             align_up((uint64_t)(numExperts + 1) * 4u, 256) + 256;
+    }
+    const int Bsort = p->passes == 1 ? (int)range : p->Bmax;
+    uint64_t sb = csort_workspace_bytes(n, Bsort) + 4 * align_up((uint64_t)n * 4u, 256);
+    if (paddedMode) sb += align_up((uint64_t)(T + 1) * 4u, 256);
+    p->ms_bytes = ms;
+    p->sort_bytes = sb;
+    p->ws_bytes = ms + sb;
+    return MR_OK;
+}
+
+static int elementwise_grid(int64_t n) {
+    const int64_t want = (n + 255) / 256;
+    const int64_t cap = (int64_t)device_sm_count() * 8;
+    return (int)(want < 1 ? 1 : (want < cap ? want : cap));
+}
+
+template <int TDT, int PDT, bool HAS_PROBS, bool PADDED>
+static cudaError_t launch_reduce(const UnpermutePlan& p, const uint8_t* permuted,
+                                 const int32_t* si, const void* pp, const int32_t* out_index,
+                                 const int32_t* ptr, uint8_t* out, cudaStream_t s) {
+    const int64_t row_bytes = p.H * p.es;
+    const bool vec_ok = (row_bytes % 16 == 0) && (reinterpret_cast<uintptr_t>(permuted) % 16 == 0) &&
+                        (reinterpret_cast<uintptr_t>(out) % 16 == 0);
+    if (vec_ok) {
+        const int64_t nvec = row_bytes / 16;
+        const int64_t max_slice = (int64_t)kRedQ * 1024;
+        const int64_t slices = (nvec + max_slice - 1) / max_slice;
+        const int64_t slice_vec = (nvec + slices - 1) / slices;
+        int64_t threads = (slice_vec + kRedQ - 1) / kRedQ;
+        threads = (threads + 31) / 32 * 32;
+        if (threads < 32) threads = 32;
+        const int64_t gx = p.T < 0x7fffffff ? p.T : 0x7fffffff;
+        return launch_pdl(unpermute_reduce_vec_kernel<TDT, PDT, HAS_PROBS, PADDED>,
+                          dim3((unsigned)gx, (unsigned)slices), dim3((unsigned)threads), 0, s,
+                          permuted, p.rows, row_bytes, nvec, slice_vec, si, p.topk, pp, out_index,
+                          ptr, p.T, out);
+    }
+    int64_t threads = p.H < 256 ? (p.H + 31) / 32 * 32 : 256;
+    const int64_t gx = p.T < 0x7fffffff ? p.T : 0x7fffffff;
+    return launch_pdl(unpermute_reduce_scalar_kernel<TDT, PDT, HAS_PROBS, PADDED>, dim3((unsigned)gx),
+                      dim3((unsigned)threads), 0, s, permuted, p.rows, p.H, si, p.topk, pp,
+                      out_index, ptr, p.T, out);
+}
+
+template <int TDT, int PDT>
+static cudaError_t dispatch_reduce(const UnpermutePlan& p, const uint8_t* permuted,
+                                   const int32_t* si, const void* pp, const int32_t* out_index,
+                                   const int32_t* ptr, uint8_t* out, cudaStream_t s) {
+    if (p.probs) {
+        return p.padded ? launch_reduce<TDT, PDT, true, true>(p, permuted, si, pp, out_index, ptr, out, s)
+                        : launch_reduce<TDT, PDT, true, false>(p, permuted, si, pp, out_index, ptr, out, s);
+    }
+    return p.padded ? launch_reduce<TDT, PDT, false, true>(p, permuted, si, pp, out_index, ptr, out, s)
+                    : launch_reduce<TDT, PDT, false, false>(p, permuted, si, pp, out_index, ptr, out, s);
+}
+
+}  // namespace mr
+
+using namespace mr;
+
+extern "C" mr_status moe_unpermute_get_workspace_size(int64_t permutedRows, int64_t hidden,
+                                                       int32_t tokenDtype, int64_t numSortedIndices,
+                                                       int32_t hasProbs, int32_t probsDtype,
+                                                       int64_t numTokens, int64_t numExperts,
+                                                       int32_t paddedMode,
+                                                       const int64_t* restoreShape,
+                                                       uint64_t* workspaceSize) {
+    if (!workspaceSize) return MR_ERR_PARAM_NULLPTR;
+    UnpermutePlan p;
+    const mr_status st = plan_unpermute(permutedRows, hidden, tokenDtype, numSortedIndices,
+                                        hasProbs, probsDtype, numTokens, numExperts, paddedMode,
+                                        restoreShape, &p);
+    if (st != MR_OK) return st;
+    *workspaceSize = p.ws_bytes;
+    return MR_OK;
+}
+
+extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* sortedIndices,
+                                   const int8_t* routingMap, const void* probs,
+                                   int64_t permutedRows, int64_t hidden, int32_t tokenDtype,
+                                   int64_t numSortedIndices, int32_t probsDtype, int64_t numTokens,
+                                   int64_t numExperts, int32_t paddedMode,
+                                   const int64_t* restoreShape, void* unpermutedTokens,
+                                   int32_t* outIndex, int32_t* permuteTokenId, void* permuteProbs,
+                                   void* workspace, uint64_t workspaceSize, void* stream) {
+    if ((probs == nullptr) != (routingMap == nullptr)) return MR_ERR_PARAM_INVALID;
+    const int32_t hasProbs = probs != nullptr ? 1 : 0;
+    UnpermutePlan p;
+    mr_status st = plan_unpermute(permutedRows, hidden, tokenDtype, numSortedIndices, hasProbs,
+                                  probsDtype, numTokens, numExperts, paddedMode, restoreShape, &p);
+    if (st != MR_OK) return st;
+    if (!permutedTokens || !sortedIndices || !unpermutedTokens || !outIndex || !permuteTokenId)
+        return MR_ERR_PARAM_NULLPTR;
+    if (hasProbs && !permuteProbs) return MR_ERR_PARAM_NULLPTR;
+    if (!workspace && p.ws_bytes > 0) return MR_ERR_PARAM_NULLPTR;
+    if (workspaceSize < p.ws_bytes) return MR_ERR_WORKSPACE;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* wp = reinterpret_cast<uint8_t*>(workspace);
+    uint8_t* pp = reinterpret_cast<uint8_t*>(permuteProbs);
+
+    profile_mark(s, 4);
+    // ---- permuteProbs --------------------------------------------------------
+    if (p.probs && !p.padded) {
+        const int64_t nblk = (p.T + 31) / 32;
+        const int64_t items = nblk * p.Eu;
+        uint8_t* q = wp;
+        uint32_t* masks = reinterpret_cast<uint32_t*>(q);
+        q += align_up((uint64_t)items * 4u, 256);
+        uint32_t* offs = reinterpret_cast<uint32_t*>(q);
+        q += align_up((uint64_t)items * 4u, 256);
+        uint32_t* totals = reinterpret_cast<uint32_t*>(q);
+        q += align_up((uint64_t)p.Eu * 4u, 256);
+        uint32_t* bstart = reinterpret_cast<uint32_t*>(q);
+        q += align_up((uint64_t)(p.Eu + 1) * 4u, 256);
+        uint32_t* ticket = reinterpret_cast<uint32_t*>(q);
+        MR_TRY_CUDA(launch_pdl(mask_columns_kernel, dim3(elementwise_grid(items)), dim3(256), 0, s,
+                               routingMap, p.T, p.Eu, masks, offs, ticket));
+        const int pblocks = (int)((p.Eu + kPrefixBuckets - 1) / kPrefixBuckets);
+        GroupListOut none{nullptr, nullptr, 0};
+        MR_TRY_CUDA(launch_pdl(csort_prefix_kernel, dim3(pblocks), dim3(kPrefixBuckets * kPrefixGroups),
+                               0, s, offs, nblk, (int)p.Eu, totals, bstart, ticket, none));
+        const int64_t work = items > p.n ? items : p.n;
+        MR_TRY_CUDA(launch_pdl(mask_scatter_kernel, dim3(elementwise_grid(work)), dim3(256), 0, s,
+                               (const uint32_t*)masks, (const uint32_t*)offs, (const uint32_t*)bstart,
+                               p.T, p.Eu, p.n, reinterpret_cast<const uint8_t*>(probs), p.pes, pp));
+    } else if (p.probs && p.padded) {
+        MR_TRY_CUDA(launch_pdl(padded_probs_kernel, dim3(elementwise_grid(p.n)), dim3(256), 0, s,
+                               sortedIndices, p.n, p.T, p.Eu, p.cap,
+                               reinterpret_cast<const uint8_t*>(probs), p.pes, pp));
+    }
+
+    // ---- stable sort of sortedIndices -> outIndex, permuteTokenId ----------
+    uint8_t* q = wp + p.ms_bytes;
+    const int Bsort = p.passes == 1 ? (int)p.key_range : p.Bmax;
+    CsortBufs cs = csort_carve(q, p.n, Bsort);
+    uint32_t* keys[2];
+    int32_t* idx[2];
+    keys[0] = reinterpret_cast<uint32_t*>(q);
+    q += align_up((uint64_t)p.n * 4u, 256);
+    keys[1] = reinterpret_cast<uint32_t*>(q);
+    q += align_up((uint64_t)p.n * 4u, 256);
+    idx[0] = reinterpret_cast<int32_t*>(q);
+    q += align_up((uint64_t)p.n * 4u, 256);
+    idx[1] = reinterpret_cast<int32_t*>(q);
+    q += align_up((uint64_t)p.n * 4u, 256);
+    int32_t* ptr = p.padded ? reinterpret_cast<int32_t*>(q) : nullptr;
+
+    const int64_t limit = p.padded ? p.T : p.rows;
+    const uint32_t* kin = nullptr;
+    const int32_t* iin = nullptr;
+    for (int pass = 0; pass < p.passes; ++pass) {
+        const int B = p.passes == 1 ? (int)p.key_range : (1 << p.bits[pass]);
+        const uint32_t mask = p.passes == 1 ? 0xffffffffu : (uint32_t)((1u << p.bits[pass]) - 1u);
+        RadixKey kf{sortedIndices, kin, limit, p.padded ? 1 : 0, p.shift[pass], mask};
+        GroupListOut none{nullptr, nullptr, 0};
+        MR_TRY_CUDA(csort_run(kf, p.n, B, cs, none, s));
+        const bool last = pass == p.passes - 1;
+        MR_TRY_CUDA(launch_pdl(radix_scatter_kernel, dim3(elementwise_grid(p.n)), dim3(256), 0, s, kf,
+                               p.n, B, cs, iin, keys[pass & 1], last ? nullptr : idx[pass & 1],
+                               last ? outIndex : nullptr, last ? permuteTokenId : nullptr,
+                               p.topk > 0 ? p.topk : (int64_t)1));
+        kin = keys[pass & 1];
+        iin = idx[pass & 1];
+    }
+    if (p.padded) {
+        MR_TRY_CUDA(launch_pdl(csr_from_keys_kernel, dim3(elementwise_grid(p.n + 1)), dim3(256), 0, s,
+                               kin, p.n, p.T, ptr));
+    }
+    profile_mark(s, 5);
+
+    // ---- gather-reduce --------------------------------------------------------
+    profile_mark(s, 6);
+    const uint8_t* permuted = reinterpret_cast<const uint8_t*>(permutedTokens);
+    uint8_t* out = reinterpret_cast<uint8_t*>(unpermutedTokens);
+    cudaError_t e = cudaSuccess;
+    switch (p.tdt * 4 + p.pdt) {
+        case MR_DTYPE_F16 * 4 + MR_DTYPE_F16:
+            e = dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, s);
+            break;
+        case MR_DTYPE_F16 * 4 + MR_DTYPE_F32:
+            e = dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, s);
+            break;
+        case MR_DTYPE_BF16 * 4 + MR_DTYPE_BF16:
+            e = dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_BF16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, s);
+            break;
+        case MR_DTYPE_BF16 * 4 + MR_DTYPE_F32:
+            e = dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, s);
+            break;
+        case MR_DTYPE_F32 * 4 + MR_DTYPE_F32:
+            e = dispatch_reduce<MR_DTYPE_F32, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, s);
+            break;
+        default:
+            return MR_ERR_PARAM_INVALID;
+    }
+    MR_TRY_CUDA(e);
+    profile_mark(s, 7);
+    MR_TRY_CUDA(cudaGetLastError());
+    return MR_OK;
+}
