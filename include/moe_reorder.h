@@ -146,6 +146,37 @@ mr_status ffnwb_batching(const int32_t* expertIds, int32_t layerId, const void* 
                          int64_t* actualTokenNum, int32_t* sortedIndicesOut, void* workspace,
                          uint64_t workspaceSize, void* stream);
 
+/*
+ * ffnwb_batching_noalloc -- the batching for callers that cannot allocate.
+ *   No counterpart on the pages: the pages' two-stage calls always take a
+ *   caller-allocated workspace. Some callers cannot allocate device memory
+ *   when they call, e.g. a plugin inside an engine that reserved all device
+ *   memory at start-up, or a latency-critical loop that cannot afford
+ *   cudaMalloc's implicit synchronisation. This entry point computes exactly
+ *   what ffnwb_batching computes, with the same arguments minus the workspace,
+ *   and allocates nothing: its scratch is a fixed array of
+ *   MR_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that
+ *   loads the library holds until the process exits.
+ *   - Calls that need more scratch than the array holds return
+ *     MR_ERR_WORKSPACE (4 MiB covers, e.g., Y = 147456 slots with
+ *     expertNum = 8192, or Y = 262144 slots with expertNum = 1024).
+ *   - All calls on a device share the array: calls whose work overlaps on the
+ *     GPU (e.g. two streams at once) race; order them.
+ *   - The first call on a device looks up the array's address on that device
+ *     and caches it; make that first call before any stream capture.
+ *   Returns the codes of ffnwb_batching.
+ */
+#define MR_NOALLOC_SCRATCH_BYTES (4u * 1024u * 1024u)
+mr_status ffnwb_batching_noalloc(const int32_t* expertIds, int32_t layerId, const void* tokenData,
+                                 int64_t tokenRowStride, const void* scales, int64_t scaleStride,
+                                 const int32_t* sessionIdsIn, const int32_t* microBatchIdsIn,
+                                 const int32_t* tokenIdsIn, int64_t expertNum,
+                                 const int64_t* maxOutShape, int64_t tokenDtype,
+                                 int64_t needSchedule, int64_t layerNum, void* y,
+                                 int64_t* groupList, int32_t* sessionIds, int32_t* microBatchIds,
+                                 int32_t* tokenIds, int32_t* expertOffsets, float* dynamicScale,
+                                 int64_t* actualTokenNum, int32_t* sortedIndicesOut, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Routing-map unpermute                                                    */
 /* ------------------------------------------------------------------------ */
