@@ -385,14 +385,14 @@ def run_ours(args):
     sec_step = max_over_ranks(sec_step, world, dev)
 
     # ---- per-phase kernel times (library phase events on the launch stream) ----
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
-    phase = {p: [] for p in range(4)}
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
+    phase = {p: [] for p in range(5)}
     usc.profile_set_events(ev)
     try:
         for _ in range(args.steps):
             step()
             torch.cuda.synchronize()
-            for p in range(4):
+            for p in range(5):
                 phase[p].append(ev[2 * p].elapsed_time(ev[2 * p + 1]) / 1e3)
     finally:
         usc.profile_set_events(None)
@@ -466,6 +466,7 @@ def run_ours(args):
             "batching_index_ms": ph[0] * 1e3, "batching_gather_ms": ph[1] * 1e3,
             "batching_gather_gbs": gather_gbs,
             "unpermute_index_ms": ph[2] * 1e3, "unpermute_reduce_ms": ph[3] * 1e3,
+            "unpermute_sort_ms_concurrent": ph[4] * 1e3,
             "unpermute_reduce_gbs": reduce_gbs, "unpermute_reduce_frac": reduce_gbs / peak,
             "batching_gbs": ab["batching"] / (ph[0] + ph[1]) / 1e9,
             "unpermute_gbs": ab["unpermute"] / (ph[2] + ph[3]) / 1e9},

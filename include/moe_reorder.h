@@ -16,7 +16,10 @@
  *  - Pointers named as device pointers must point to device memory of the
  *    current CUDA device; pointers named host pointers to host memory.
  *  - The caller owns and frees every buffer, including the workspace. The
- *    library allocates no device memory and keeps no per-call state.
+ *    library allocates no device memory and keeps no per-call state. The
+ *    not-padded moe_unpermute keeps one auxiliary stream and two events per
+ *    device (created on first use, kept until exit): its sort of
+ *    sortedIndices runs there, forked from and joined back into `stream`.
  *  - Execute calls are asynchronous on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream). Outputs are valid once the caller synchronises
  *    the stream. Nothing is read back to the host.
@@ -272,8 +275,10 @@ int32_t mr_version(void);
  *   NULL / 0 to switch timing off. While set, the calling thread's execute
  *   calls record events[2p] before and events[2p+1] after phase p on their
  *   stream, phases being: 0 batching index build, 1 batching row gather,
- *   2 unpermute index work (maskedSelect / probs lookup and the sort),
- *   3 unpermute gather-reduce. Phases beyond `count/2` are not recorded.
+ *   2 unpermute probs work (maskedSelect or the padded lookup; padded: also
+ *   the sort), 3 unpermute gather-reduce, 4 the not-padded sort, which runs
+ *   on the library's auxiliary stream (its events are recorded there).
+ *   Phases beyond `count/2` are not recorded.
  *   The setting is per host thread. Returns MR_OK or MR_ERR_PARAM_INVALID.
  */
 mr_status mr_profile_set_events(void* const* events, int32_t count);

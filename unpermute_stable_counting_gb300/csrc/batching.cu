@@ -41,7 +41,7 @@ batching_scatter_kernel(BatchKey kf, int64_t Y, int B, CsortBufs cs,
                         int32_t* __restrict__ micro_out, int32_t* __restrict__ tok_out,
                         int32_t* __restrict__ eoff_out, int32_t* __restrict__ gather_idx,
                         int32_t* __restrict__ slot_row) {
-    grid_dependency_wait();
+    pdl_enter();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < Y; s += stride) {
         const int k = kf(s);
@@ -64,7 +64,11 @@ batching_scatter_kernel(BatchKey kf, int64_t Y, int B, CsortBufs cs,
 }
 
 // Copy `bytes` from src to dst with one warp. Vector width follows the common
-// alignment of both addresses and the length.
+// alignment of both addresses and the length: 16-byte vectors (VPT in flight
+// per lane), else 4-byte words, else bytes. Addresses are formed from the
+// __restrict__ row pointers directly, which leaves the compiler free to start
+// the next batch's loads before the current stores (measured on GB300: 616 us
+// against 626 us for the round-trip gather with pointer casts).
 template <int VPT>
 __device__ __forceinline__ void warp_copy_row(const uint8_t* __restrict__ src,
                                               uint8_t* __restrict__ dst, int64_t bytes, int lane) {
@@ -111,7 +115,7 @@ batching_gather_kernel(const uint8_t* __restrict__ token_data, int64_t row_strid
                        int64_t scale_stride, uint8_t* __restrict__ y, float* __restrict__ dyn,
                        const int32_t* __restrict__ gather_idx,
                        const uint32_t* __restrict__ bucket_start, int E) {
-    grid_dependency_wait();
+    pdl_enter();
     const uint32_t U = bucket_start[E];
     const int lane = threadIdx.x & 31;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -170,6 +174,7 @@ static mr_status plan_batching(int64_t expertNum, const int64_t* maxOutShape, in
     p->ws_bytes = csort_workspace_bytes(p->Y, p->B) + align_up((uint64_t)p->Y * 4u, 256);
     return MR_OK;
 }
+
 
 static int gather_grid(int64_t rows) {
     static int blocks_per_sm[64] = {0};

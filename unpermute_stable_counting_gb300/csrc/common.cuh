@@ -6,6 +6,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/moe_reorder.h"
 
 namespace mr {
@@ -13,10 +15,11 @@ namespace mr {
 constexpr int kNumSMsHint = 152;  // GB300; the launch code queries the real count
 
 // ---------------------------------------------------------------------------
-// Programmatic dependent launch. Every kernel of the library calls
-// grid_dependency_wait() before its first global-memory access, so a kernel
-// launched early (programmatic stream serialisation) never reads or writes
-// memory that the previous kernel in the stream still uses.
+// Programmatic dependent launch. Every kernel of the library starts with
+// pdl_enter(): it waits for the previous kernel in the stream before its first
+// global-memory access, so a kernel launched early (programmatic stream
+// serialisation) never reads or writes memory that the previous kernel still
+// uses.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void grid_dependency_wait() {
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -24,6 +27,10 @@ __device__ __forceinline__ void grid_dependency_wait() {
 __device__ __forceinline__ void allow_dependents() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
+// Kernel prologue: wait for the previous kernel in the stream to finish (its
+// memory is then visible). The next kernel is not triggered early: measured on
+// GB300, letting the chain of small index kernels launch early made it slower.
+__device__ __forceinline__ void pdl_enter() { grid_dependency_wait(); }
 
 // ---------------------------------------------------------------------------
 // Cache-hinted global accesses for streamed data (read once / written once).
@@ -124,6 +131,17 @@ __device__ __forceinline__ float load_f32(const void* base, int64_t i, int dt) {
 inline uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 int device_sm_count();                 // cached per device
+
+// Per-device auxiliary stream with fork/join events, created on first use and
+// kept for the process lifetime. `mu` serialises the enqueue of one fork/join
+// sequence, so concurrent host threads do not interleave their records.
+struct AuxStream {
+    cudaStream_t stream;
+    cudaEvent_t fork;
+    cudaEvent_t join;
+    std::mutex mu;
+};
+AuxStream* aux_stream();  // for the current device; nullptr on a CUDA error
 void profile_mark(cudaStream_t s, int event_index);  // records a timing event if set
 
 // Launch with programmatic stream serialisation (PDL) enabled.

@@ -9,9 +9,10 @@
 //   rank   kernel: per tile of kSortTile items, the stable rank of each item
 //                  among the items of the tile with the same key, and the
 //                  tile's histogram (tile-major matrix [tiles][B]).
-//   prefix kernel: per bucket, the exclusive prefix of the histogram over the
-//                  tiles (in place), the bucket totals, and -- in the block
-//                  that finishes last -- the exclusive scan of the totals
+//   prefix kernel: per bucket (one warp each), the exclusive prefix of the
+//                  histogram over the tiles (in place), the bucket totals,
+//                  and -- in the block that finishes last -- the exclusive
+//                  scan of the totals
 //                  (bucket_start) plus an optional compacted
 //                  [key, count] list of the non-empty buckets below a limit.
 //   consumers:     elementwise kernels of each operation call csort_dest().
@@ -37,8 +38,10 @@ constexpr int kSortThreads = kSortWarps * 32;
 constexpr int kSortChunks = 8;  // 32-item chunks per warp
 constexpr int kSortTile = kSortWarps * 32 * kSortChunks;  // 2048 items per tile
 constexpr int kMaxBuckets = 8193;                          // expertNum <= 8192, plus the sentinel
-constexpr int kPrefixBuckets = 32;                         // buckets per prefix block
-constexpr int kPrefixGroups = 8;                           // tile groups per prefix block
+constexpr int kPrefixWarps = 8;                            // keys per prefix block (one per warp)
+constexpr int kPrefixThreads = kPrefixWarps * 32;
+constexpr int kPrefixPrefetch = 4;                         // 32-tile steps loaded together
+constexpr int kLastChunk = 8;                              // key totals per load batch (last block)
 
 // At least one tile, so an empty input still produces zero totals.
 inline int64_t csort_tiles(int64_t N) { return N > 0 ? (N + kSortTile - 1) / kSortTile : 1; }
@@ -80,7 +83,7 @@ __global__ void __launch_bounds__(kSortThreads)
 csort_rank_kernel(KeyFn kf, int64_t N, int B, uint16_t* __restrict__ tile_rank,
                   uint32_t* __restrict__ tile_counts, uint32_t* __restrict__ ticket) {
     extern __shared__ __align__(16) uint16_t tab[];  // [kSortWarps][B] per-warp key counters
-    grid_dependency_wait();
+    pdl_enter();
     if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
 
     const int tab_words = (kSortWarps * B + 1) / 2;
@@ -142,48 +145,44 @@ struct GroupListOut {
     int limit;
 };
 
-static __global__ void __launch_bounds__(kPrefixBuckets * kPrefixGroups)
+static __global__ void __launch_bounds__(kPrefixThreads)
 csort_prefix_kernel(uint32_t* __restrict__ tile_off, int64_t tiles, int B,
                     uint32_t* __restrict__ totals, uint32_t* __restrict__ bucket_start,
                     uint32_t* __restrict__ ticket, GroupListOut gl) {
-    __shared__ uint32_t part[kPrefixGroups][kPrefixBuckets + 1];
     __shared__ uint32_t warp_sums[32];
     __shared__ int is_last;
-    grid_dependency_wait();
+    pdl_enter();
 
-    const int x = threadIdx.x % kPrefixBuckets;
-    const int g = threadIdx.x / kPrefixBuckets;
-    const int b = blockIdx.x * kPrefixBuckets + x;
-    const int64_t per = (tiles + kPrefixGroups - 1) / kPrefixGroups;
-    const int64_t t0 = g * per;
-    const int64_t t1 = t0 + per < tiles ? t0 + per : tiles;
-
-    uint32_t sum = 0u;
+    // One warp per key: an exclusive scan of the key's tile counts, 32 tiles
+    // per step (lane = tile), kPrefixPrefetch steps of loads issued together.
+    const int lane = threadIdx.x & 31;
+    const int b = blockIdx.x * kPrefixWarps + (threadIdx.x >> 5);
     if (b < B) {
-        for (int64_t t = t0; t < t1; ++t) sum += tile_off[t * B + b];
-    }
-    part[g][x] = sum;
-    __syncthreads();
-    if (g == 0) {
-        uint32_t run = 0u;
-        for (int q = 0; q < kPrefixGroups; ++q) {
-            const uint32_t v = part[q][x];
-            part[q][x] = run;
-            run += v;
+        uint32_t carry = 0u;
+        for (int64_t t0 = 0; t0 < tiles; t0 += 32 * kPrefixPrefetch) {
+            uint32_t v[kPrefixPrefetch];
+#pragma unroll
+            for (int u = 0; u < kPrefixPrefetch; ++u) {
+                const int64_t t = t0 + 32 * u + lane;
+                v[u] = t < tiles ? tile_off[t * B + b] : 0u;
+            }
+#pragma unroll
+            for (int u = 0; u < kPrefixPrefetch; ++u) {
+                uint32_t incl = v[u];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(0xffffffffu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                const int64_t t = t0 + 32 * u + lane;
+                if (t < tiles) tile_off[t * B + b] = carry + incl - v[u];
+                carry += __shfl_sync(0xffffffffu, incl, 31);
+            }
         }
-        if (b < B) totals[b] = run;
-    }
-    __syncthreads();
-    if (b < B) {
-        uint32_t run = part[g][x];
-        for (int64_t t = t0; t < t1; ++t) {
-            const uint32_t c = tile_off[t * B + b];
-            tile_off[t * B + b] = run;
-            run += c;
-        }
+        if (lane == 0) totals[b] = carry;
     }
 
-    // The block that finishes last scans the bucket totals.
+    // The block that finishes last scans the key totals.
     __threadfence();
     __syncthreads();
     if (threadIdx.x == 0) is_last = atomicAdd(ticket, 1u) == gridDim.x - 1 ? 1 : 0;
@@ -191,42 +190,65 @@ csort_prefix_kernel(uint32_t* __restrict__ tile_off, int64_t tiles, int B,
     if (!is_last) return;
     __threadfence();
 
-    const int nthr = blockDim.x;
-    const int per_t = (B + nthr - 1) / nthr;
+    // Each thread owns a run of per_t consecutive keys, read kLastChunk at a
+    // time with the loads of a chunk issued together.
+    const int per_t = (B + kPrefixThreads - 1) / kPrefixThreads;
     const int c0 = threadIdx.x * per_t;
     const int c1 = c0 + per_t < B ? c0 + per_t : B;
     uint32_t s = 0u, ng = 0u;
-    for (int i = c0; i < c1; ++i) {
-        const uint32_t v = __ldcg(&totals[i]);
-        s += v;
-        if (i < gl.limit && v != 0u) ++ng;
+    for (int i0 = c0; i0 < c1; i0 += kLastChunk) {
+        uint32_t v[kLastChunk];
+#pragma unroll
+        for (int q = 0; q < kLastChunk; ++q) v[q] = i0 + q < c1 ? __ldcg(&totals[i0 + q]) : 0u;
+#pragma unroll
+        for (int q = 0; q < kLastChunk; ++q) {
+            s += v[q];
+            if (i0 + q < c1 && i0 + q < gl.limit && v[q] != 0u) ++ng;
+        }
     }
     uint32_t total_all = 0u, groups = 0u;
     const uint32_t excl = block_exclusive_scan(s, warp_sums, &total_all);
     const uint32_t gexcl = block_exclusive_scan(ng, warp_sums, &groups);
     uint32_t run = excl, r = gexcl;
-    for (int i = c0; i < c1; ++i) {
-        const uint32_t v = __ldcg(&totals[i]);
-        bucket_start[i] = run;
-        if (gl.rows && i < gl.limit && v != 0u) {
-            gl.rows[2 * (int64_t)r] = i;
-            gl.rows[2 * (int64_t)r + 1] = v;
-            ++r;
+    for (int i0 = c0; i0 < c1; i0 += kLastChunk) {
+        uint32_t v[kLastChunk];
+#pragma unroll
+        for (int q = 0; q < kLastChunk; ++q) v[q] = i0 + q < c1 ? __ldcg(&totals[i0 + q]) : 0u;
+#pragma unroll
+        for (int q = 0; q < kLastChunk; ++q) {
+            const int i = i0 + q;
+            if (i < c1) {
+                bucket_start[i] = run;
+                if (gl.rows && i < gl.limit && v[q] != 0u) {
+                    gl.rows[2 * (int64_t)r] = i;
+                    gl.rows[2 * (int64_t)r + 1] = v[q];
+                    ++r;
+                }
+                run += v[q];
+            }
         }
-        run += v;
     }
     if (threadIdx.x == 0) {
         bucket_start[B] = total_all;
         *ticket = 0u;
     }
     if (gl.rows) {
-        for (int64_t q = (int64_t)groups + threadIdx.x; q < gl.limit; q += nthr) {
+        for (int64_t q = (int64_t)groups + threadIdx.x; q < gl.limit; q += kPrefixThreads) {
             gl.rows[2 * q] = 0;
             gl.rows[2 * q + 1] = 0;
         }
     }
     __syncthreads();
     if (gl.count_out && threadIdx.x == 0) *gl.count_out = (int64_t)bucket_start[gl.limit];
+}
+
+// Launch of the prefix kernel over a [tiles][B] count matrix.
+inline cudaError_t csort_prefix(uint32_t* tile_off, int64_t tiles, int B, uint32_t* totals,
+                                uint32_t* bucket_start, uint32_t* ticket, GroupListOut gl,
+                                cudaStream_t st) {
+    const int blocks = (B + kPrefixWarps - 1) / kPrefixWarps;
+    return launch_pdl(csort_prefix_kernel, dim3(blocks), dim3(kPrefixThreads), 0, st, tile_off,
+                      tiles, B, totals, bucket_start, ticket, gl);
 }
 
 // Position of item i (key k) in the stable order.
@@ -250,9 +272,7 @@ inline cudaError_t csort_run(KeyFn kf, int64_t N, int B, const CsortBufs& b, Gro
                                dim3(kSortThreads), smem, st, kf, N, B, b.tile_rank, b.tile_off,
                                b.ticket);
     if (e != cudaSuccess) return e;
-    const int pblocks = (B + kPrefixBuckets - 1) / kPrefixBuckets;
-    return launch_pdl(csort_prefix_kernel, dim3(pblocks), dim3(kPrefixBuckets * kPrefixGroups), 0,
-                      st, b.tile_off, tiles, B, b.totals, b.bucket_start, b.ticket, gl);
+    return csort_prefix(b.tile_off, tiles, B, b.totals, b.bucket_start, b.ticket, gl, st);
 }
 
 }  // namespace mr

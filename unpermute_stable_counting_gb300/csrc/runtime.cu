@@ -21,6 +21,27 @@ int device_sm_count() {
     return n;
 }
 
+AuxStream* aux_stream() {
+    static std::mutex create_mu;
+    static AuxStream* streams[64] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+    std::lock_guard<std::mutex> lock(create_mu);
+    if (!streams[dev]) {
+        int lo = 0, hi = 0;
+        if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return nullptr;
+        AuxStream* a = new AuxStream();
+        if (cudaStreamCreateWithPriority(&a->stream, cudaStreamNonBlocking, hi) != cudaSuccess ||
+            cudaEventCreateWithFlags(&a->fork, cudaEventDisableTiming) != cudaSuccess ||
+            cudaEventCreateWithFlags(&a->join, cudaEventDisableTiming) != cudaSuccess) {
+            delete a;
+            return nullptr;
+        }
+        streams[dev] = a;
+    }
+    return streams[dev];
+}
+
 void profile_mark(cudaStream_t s, int event_index) {
     if (event_index < g_num_events && g_events[event_index]) cudaEventRecord(g_events[event_index], s);
 }

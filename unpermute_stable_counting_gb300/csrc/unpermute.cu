@@ -11,11 +11,14 @@
 //   always            : stable sort of sortedIndices (1-3 LSD passes of the
 //                       counting-sort engine) -> outIndex, permuteTokenId;
 //                       padded: per-token row ranges (CSR) from the sorted keys
-//   always            : gather-reduce, one CTA per (token, hidden slice),
+//   not padded        : the sort runs on the library's auxiliary stream,
+//                       overlapping the gather-reduce (fork/join events)
+//   always            : gather-reduce, one warp per (token, hidden chunk),
 //                       fp32 accumulation in ascending slot / row order,
 //                       atomic-free, one RNE cast per output element.
 #include <cstdio>
 #include <cstdlib>
+#include <mutex>
 
 #include "csort.cuh"
 
@@ -43,52 +46,68 @@ __global__ void __launch_bounds__(256)
 mask_columns_kernel(const int8_t* __restrict__ map, int64_t T, int64_t Eu,
                     uint32_t* __restrict__ masks, uint32_t* __restrict__ counts,
                     uint32_t* __restrict__ ticket) {
-    grid_dependency_wait();
+    pdl_enter();
     if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
+    // one warp per 32-token block; lane j reads token t0+j; a ballot per expert
+    const int lane = threadIdx.x & 31;
     const int64_t nblk = (T + 31) / 32;
-    const int64_t items = nblk * Eu;
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < items; it += stride) {
-        const int64_t blk = it / Eu;
-        const int64_t e = it - blk * Eu;
-        const int64_t t0 = blk * 32;
-        const int nt = (int)(T - t0 < 32 ? T - t0 : 32);
-        uint32_t bits = 0u;
-        for (int j = 0; j < nt; ++j) bits |= (map[(t0 + j) * Eu + e] != 0 ? 1u : 0u) << j;
-        masks[it] = bits;
-        counts[it] = __popc(bits);
-    }
-}
-
-__global__ void __launch_bounds__(256)
-mask_scatter_kernel(const uint32_t* __restrict__ masks, const uint32_t* __restrict__ offs,
-                    const uint32_t* __restrict__ bucket_start, int64_t T, int64_t Eu, int64_t n,
-                    const uint8_t* __restrict__ probs, int pes, uint8_t* __restrict__ pp) {
-    grid_dependency_wait();
-    const int64_t nblk = (T + 31) / 32;
-    const int64_t items = nblk * Eu;
-    const int64_t nnz = bucket_start[Eu];
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const int64_t total = items > n ? items : n;
-    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total; it += stride) {
-        if (it < items) {
-            uint32_t bits = masks[it];
-            if (bits) {
-                const int64_t blk = it / Eu;
-                const int64_t e = it - blk * Eu;
-                int64_t pos = (int64_t)bucket_start[e] + offs[it];
-                while (bits && pos < n) {
-                    const int j = __ffs(bits) - 1;
-                    bits &= bits - 1u;
-                    const int64_t src = ((blk * 32 + j) * Eu + e) * pes;
-                    for (int b = 0; b < pes; ++b) pp[pos * pes + b] = probs[src + b];
-                    ++pos;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t blk = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; blk < nblk;
+         blk += nwarps) {
+        const int64_t t = blk * 32 + lane;
+        const int8_t* row = map + t * Eu;
+        for (int64_t e0 = 0; e0 < Eu; e0 += 8) {
+            int8_t m[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) m[u] = (t < T && e0 + u < Eu) ? row[e0 + u] : (int8_t)0;
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const uint32_t bits = __ballot_sync(0xffffffffu, m[u] != 0);
+                if (lane == u && e0 + u < Eu) {
+                    masks[blk * Eu + e0 + u] = bits;
+                    counts[blk * Eu + e0 + u] = __popc(bits);
                 }
             }
         }
-        if (it >= nnz && it < n) {
-            for (int b = 0; b < pes; ++b) pp[it * pes + b] = 0;
+    }
+}
+
+// Copy one element of 2 or 4 bytes (the probs dtype) without interpreting it.
+__device__ __forceinline__ void copy_prob(uint8_t* dst, int64_t di, const uint8_t* src, int64_t si,
+                                          int pes) {
+    if (pes == 4) {
+        reinterpret_cast<uint32_t*>(dst)[di] = __ldg(reinterpret_cast<const uint32_t*>(src) + si);
+    } else {
+        reinterpret_cast<uint16_t*>(dst)[di] = __ldg(reinterpret_cast<const unsigned short*>(src) + si);
+    }
+}
+__device__ __forceinline__ void zero_prob(uint8_t* dst, int64_t di, int pes) {
+    if (pes == 4) reinterpret_cast<uint32_t*>(dst)[di] = 0u;
+    else reinterpret_cast<uint16_t*>(dst)[di] = 0;
+}
+
+// One thread per (token, expert) element: a routed element lands at
+// bucket_start[e] + offs[blk][e] + (routed tokens of its block below it).
+__global__ void __launch_bounds__(256)
+mask_scatter_kernel(const int8_t* __restrict__ map, const uint32_t* __restrict__ masks,
+                    const uint32_t* __restrict__ offs, const uint32_t* __restrict__ bucket_start,
+                    int64_t T, int64_t Eu, int64_t n, const uint8_t* __restrict__ probs, int pes,
+                    uint8_t* __restrict__ pp) {
+    pdl_enter();
+    const int64_t N = T * Eu;
+    const int64_t nnz = bucket_start[Eu];
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t total = N > n ? N : n;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
+        if (i < N && map[i] != 0) {
+            const int64_t t = i / Eu;
+            const int64_t e = i - t * Eu;
+            const int64_t item = (t >> 5) * Eu + e;
+            const uint32_t below = masks[item] & ((1u << (t & 31)) - 1u);
+            const int64_t pos = (int64_t)bucket_start[e] + offs[item] + __popc(below);
+            if (pos < n) copy_prob(pp, pos, probs, i, pes);
         }
+        if (i >= nnz && i < n) zero_prob(pp, i, pes);
     }
 }
 
@@ -96,15 +115,14 @@ mask_scatter_kernel(const uint32_t* __restrict__ masks, const uint32_t* __restri
 __global__ void __launch_bounds__(256)
 padded_probs_kernel(const int32_t* __restrict__ si, int64_t n, int64_t T, int64_t Eu, int64_t cap,
                     const uint8_t* __restrict__ probs, int pes, uint8_t* __restrict__ pp) {
-    grid_dependency_wait();
+    pdl_enter();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
         const int32_t v = si[i];
         if (v >= 0 && v < T) {
-            const int64_t src = ((int64_t)v * Eu + i / cap) * pes;
-            for (int b = 0; b < pes; ++b) pp[i * pes + b] = probs[src + b];
+            copy_prob(pp, i, probs, (int64_t)v * Eu + i / cap, pes);
         } else {
-            for (int b = 0; b < pes; ++b) pp[i * pes + b] = 0;
+            zero_prob(pp, i, pes);
         }
     }
 }
@@ -137,7 +155,7 @@ __global__ void __launch_bounds__(256)
 radix_scatter_kernel(RadixKey kf, int64_t n, int B, CsortBufs cs, const int32_t* __restrict__ idx_in,
                      uint32_t* __restrict__ keys_out, int32_t* __restrict__ idx_out,
                      int32_t* __restrict__ out_index, int32_t* __restrict__ ptid, int64_t topk) {
-    grid_dependency_wait();
+    pdl_enter();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
         const uint32_t fk = kf.full(i);
@@ -158,7 +176,7 @@ radix_scatter_kernel(RadixKey kf, int64_t n, int B, CsortBufs cs, const int32_t*
 __global__ void __launch_bounds__(256)
 csr_from_keys_kernel(const uint32_t* __restrict__ keys, int64_t n, int64_t T,
                      int32_t* __restrict__ ptr) {
-    grid_dependency_wait();
+    pdl_enter();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p <= n; p += stride) {
         const int64_t prev = p > 0 ? (int64_t)keys[p - 1] : -1;
@@ -169,15 +187,14 @@ csr_from_keys_kernel(const uint32_t* __restrict__ keys, int64_t n, int64_t T,
 }
 
 // ---------------------------------------------------------------------------
-// Gather-reduce. One CTA per (token, hidden slice). Warp 0 builds the
-// token's list of contributing rows in ascending order (valid index and,
-// with probs, nonzero prob) in shared memory; every thread then owns up to
-// kRedQ 16-byte output vectors and adds the rows in list order in fp32:
-// acc = acc + f32(x) * f32(p), each operation rounded on its own.
+// Gather-reduce. A token's contributing rows are those with a valid index
+// and, with probs, a nonzero prob, taken in ascending slot (not padded) or
+// row (padded) order; they are added in fp32, acc = acc + f32(x) * f32(p),
+// each operation rounded on its own, then cast once with RNE.
 // ---------------------------------------------------------------------------
-constexpr int kListCap = 512;
-constexpr int kRedUnroll = 4;
-constexpr int kRedQ = 2;
+constexpr int kListCap = 512;   // list entries per pass of the element-wise kernel
+constexpr int kRedUnroll = 4;   // rows in flight per warp step
+constexpr int kRedVQ = 2;       // 16-byte vectors per lane per work item
 
 template <bool HAS_PROBS, bool PADDED, int PDT>
 __device__ __forceinline__ int build_list(int64_t c0, int64_t c1, const int32_t* __restrict__ si,
@@ -258,21 +275,27 @@ struct Vec<MR_DTYPE_F16> : Vec16<MR_DTYPE_F16> {};
 template <>
 struct Vec<MR_DTYPE_BF16> : Vec16<MR_DTYPE_BF16> {};
 
+// One warp per work item = (token, chunk of 32*kRedVQ 16-byte vectors of the
+// hidden dimension). The warp's lanes load up to 32 of the token's slots at a
+// time (index and weight), a ballot keeps the contributing ones in ascending
+// order, and the warp adds them kRedUnroll rows at a time, each lane owning
+// kRedVQ vectors: no shared memory and no block barrier.
 template <int TDT, int PDT, bool HAS_PROBS, bool PADDED>
-__global__ void __launch_bounds__(1024)
-unpermute_reduce_vec_kernel(const uint8_t* __restrict__ permuted, int64_t rows, int64_t row_bytes,
-                            int64_t nvec, int64_t slice_vec, const int32_t* __restrict__ si,
-                            int64_t topk, const void* __restrict__ pp,
-                            const int32_t* __restrict__ out_index, const int32_t* __restrict__ ptr,
-                            int64_t T, uint8_t* __restrict__ out) {
+__global__ void __launch_bounds__(256)
+unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows, int64_t row_bytes,
+                             int64_t nvec, int64_t chunks, const int32_t* __restrict__ si,
+                             int64_t topk, const void* __restrict__ pp,
+                             const int32_t* __restrict__ out_index, const int32_t* __restrict__ ptr,
+                             int64_t T, uint8_t* __restrict__ out) {
     using V = Vec<TDT>;
-    __shared__ int64_t s_row[kListCap];
-    __shared__ float s_w[kListCap];
-    __shared__ int s_cnt;
-    grid_dependency_wait();
-    const int64_t v0 = (int64_t)blockIdx.y * slice_vec;
-    const int64_t v1 = v0 + slice_vec < nvec ? v0 + slice_vec : nvec;
-    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    pdl_enter();
+    const int lane = threadIdx.x & 31;
+    const int64_t items = T * chunks;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < items;
+         item += nw) {
+        const int64_t t = item / chunks;
+        const int64_t v0 = (item - t * chunks) * (32 * kRedVQ) + lane;
         int64_t L0, L1;
         if (PADDED) {
             L0 = ptr[t];
@@ -281,59 +304,82 @@ unpermute_reduce_vec_kernel(const uint8_t* __restrict__ permuted, int64_t rows, 
             L0 = t * topk;
             L1 = L0 + topk;
         }
-        float acc[kRedQ][V::N];
+        float acc[kRedVQ][V::N];
 #pragma unroll
-        for (int q = 0; q < kRedQ; ++q)
+        for (int q = 0; q < kRedVQ; ++q)
 #pragma unroll
             for (int k = 0; k < V::N; ++k) acc[q][k] = 0.0f;
 
-        for (int64_t c0 = L0; c0 < L1; c0 += kListCap) {
-            const int64_t c1 = c0 + kListCap < L1 ? c0 + kListCap : L1;
-            if (threadIdx.x < 32) {
-                const int cnt = build_list<HAS_PROBS, PADDED, PDT>(c0, c1, si, rows, row_bytes, pp,
-                                                                   out_index, s_row, s_w);
-                if (threadIdx.x == 0) s_cnt = cnt;
+        for (int64_t g0 = L0; g0 < L1; g0 += 32) {
+            // this lane's slot of the group: row offset and weight
+            const int64_t e = g0 + lane;
+            bool keep = false;
+            int64_t roff = 0;
+            float w = 1.0f;
+            if (e < L1) {
+                int64_t r;
+                if (PADDED) {
+                    r = out_index[e];
+                    keep = true;
+                } else {
+                    const int32_t v = si[e];
+                    keep = v >= 0 && (int64_t)v < rows;
+                    r = v;
+                }
+                if (HAS_PROBS && keep) {
+                    w = ld_f32<PDT>(pp, PADDED ? r : e);
+                    keep = w != 0.0f;
+                }
+                roff = r * row_bytes;
             }
-            __syncthreads();
-            const int cnt = s_cnt;
-            for (int m0 = 0; m0 < cnt; m0 += kRedUnroll) {
-                uint4 x[kRedUnroll][kRedQ];
+            uint32_t bal = __ballot_sync(0xffffffffu, keep);
+            while (bal) {
+                int src[kRedUnroll];
+                int cnt = 0;
 #pragma unroll
                 for (int u = 0; u < kRedUnroll; ++u) {
-                    if (m0 + u < cnt) {
-                        const uint8_t* rp = permuted + s_row[m0 + u];
+                    src[u] = bal ? __ffs(bal) - 1 : 0;
+                    if (bal) {
+                        bal &= bal - 1u;
+                        ++cnt;
+                    }
+                }
+                uint4 x[kRedUnroll][kRedVQ];
 #pragma unroll
-                        for (int q = 0; q < kRedQ; ++q) {
-                            const int64_t v = v0 + threadIdx.x + (int64_t)q * blockDim.x;
-                            if (v < v1) x[u][q] = ld_stream_v4(rp + 16 * v);
+                for (int u = 0; u < kRedUnroll; ++u) {
+                    const int64_t ro = __shfl_sync(0xffffffffu, roff, src[u]);
+                    if (u < cnt) {
+#pragma unroll
+                        for (int q = 0; q < kRedVQ; ++q) {
+                            const int64_t v = v0 + 32 * q;
+                            if (v < nvec) x[u][q] = ld_stream_v4(permuted + ro + 16 * v);
                         }
                     }
                 }
 #pragma unroll
                 for (int u = 0; u < kRedUnroll; ++u) {
-                    if (m0 + u < cnt) {
-                        const float w = s_w[m0 + u];
+                    const float wu = __shfl_sync(0xffffffffu, w, src[u]);
+                    if (u < cnt) {
 #pragma unroll
-                        for (int q = 0; q < kRedQ; ++q) {
-                            const int64_t v = v0 + threadIdx.x + (int64_t)q * blockDim.x;
-                            if (v < v1) {
+                        for (int q = 0; q < kRedVQ; ++q) {
+                            const int64_t v = v0 + 32 * q;
+                            if (v < nvec) {
                                 float xs[V::N];
                                 V::unpack(x[u][q], xs);
 #pragma unroll
                                 for (int k = 0; k < V::N; ++k)
-                                    acc[q][k] = HAS_PROBS ? __fadd_rn(acc[q][k], __fmul_rn(xs[k], w))
+                                    acc[q][k] = HAS_PROBS ? __fadd_rn(acc[q][k], __fmul_rn(xs[k], wu))
                                                           : __fadd_rn(acc[q][k], xs[k]);
                             }
                         }
                     }
                 }
             }
-            __syncthreads();
         }
 #pragma unroll
-        for (int q = 0; q < kRedQ; ++q) {
-            const int64_t v = v0 + threadIdx.x + (int64_t)q * blockDim.x;
-            if (v < v1) st_stream_v4(out + t * row_bytes + 16 * v, V::pack(acc[q]));
+        for (int q = 0; q < kRedVQ; ++q) {
+            const int64_t v = v0 + 32 * q;
+            if (v < nvec) st_stream_v4(out + t * row_bytes + 16 * v, V::pack(acc[q]));
         }
     }
 }
@@ -352,7 +398,7 @@ unpermute_reduce_scalar_kernel(const uint8_t* __restrict__ permuted, int64_t row
     __shared__ float s_w[kListCap];
     __shared__ int s_cnt;
     constexpr int es = TDT == MR_DTYPE_F32 ? 4 : 2;
-    grid_dependency_wait();
+    pdl_enter();
     const int64_t row_bytes = H * es;
     for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
         int64_t L0, L1;
@@ -540,17 +586,26 @@ static cudaError_t launch_reduce(const UnpermutePlan& p, const uint8_t* permuted
                         (reinterpret_cast<uintptr_t>(out) % 16 == 0);
     if (vec_ok) {
         const int64_t nvec = row_bytes / 16;
-        const int64_t max_slice = (int64_t)kRedQ * 1024;
-        const int64_t slices = (nvec + max_slice - 1) / max_slice;
-        const int64_t slice_vec = (nvec + slices - 1) / slices;
-        int64_t threads = (slice_vec + kRedQ - 1) / kRedQ;
-        threads = (threads + 31) / 32 * 32;
-        if (threads < 32) threads = 32;
-        const int64_t gx = p.T < 0x7fffffff ? p.T : 0x7fffffff;
-        return launch_pdl(unpermute_reduce_vec_kernel<TDT, PDT, HAS_PROBS, PADDED>,
-                          dim3((unsigned)gx, (unsigned)slices), dim3((unsigned)threads), 0, s,
-                          permuted, p.rows, row_bytes, nvec, slice_vec, si, p.topk, pp, out_index,
-                          ptr, p.T, out);
+        const int64_t chunks = (nvec + 32 * kRedVQ - 1) / (32 * kRedVQ);
+        const int64_t warps = p.T * chunks;
+        static int blocks_per_sm[64] = {0};
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int bps = dev < 64 ? blocks_per_sm[dev] : 0;
+        if (bps == 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                    &bps, unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED>, 256, 0) !=
+                    cudaSuccess || bps <= 0)
+                bps = 4;
+            if (dev < 64) blocks_per_sm[dev] = bps;
+        }
+        int64_t grid = (warps + 7) / 8;
+        const int64_t cap = (int64_t)device_sm_count() * bps;
+        if (grid > cap) grid = cap;
+        if (grid < 1) grid = 1;
+        return launch_pdl(unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED>, dim3((unsigned)grid),
+                          dim3(256), 0, s, permuted, p.rows, row_bytes, nvec, chunks, si, p.topk, pp,
+                          out_index, ptr, p.T, out);
     }
     int64_t threads = p.H < 256 ? (p.H + 31) / 32 * 32 : 256;
     const int64_t gx = p.T < 0x7fffffff ? p.T : 0x7fffffff;
@@ -616,36 +671,40 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
     uint8_t* wp = reinterpret_cast<uint8_t*>(workspace);
     uint8_t* pp = reinterpret_cast<uint8_t*>(permuteProbs);
 
-    profile_mark(s, 4);
-    // ---- permuteProbs --------------------------------------------------------
-    if (p.probs && !p.padded) {
-        const int64_t nblk = (p.T + 31) / 32;
-        const int64_t items = nblk * p.Eu;
-        uint8_t* q = wp;
-        uint32_t* masks = reinterpret_cast<uint32_t*>(q);
-        q += align_up((uint64_t)items * 4u, 256);
-        uint32_t* offs = reinterpret_cast<uint32_t*>(q);
-        q += align_up((uint64_t)items * 4u, 256);
-        uint32_t* totals = reinterpret_cast<uint32_t*>(q);
-        q += align_up((uint64_t)p.Eu * 4u, 256);
-        uint32_t* bstart = reinterpret_cast<uint32_t*>(q);
-        q += align_up((uint64_t)(p.Eu + 1) * 4u, 256);
-        uint32_t* ticket = reinterpret_cast<uint32_t*>(q);
-        MR_TRY_CUDA(launch_pdl(mask_columns_kernel, dim3(elementwise_grid(items)), dim3(256), 0, s,
-                               routingMap, p.T, p.Eu, masks, offs, ticket));
-        const int pblocks = (int)((p.Eu + kPrefixBuckets - 1) / kPrefixBuckets);
-        GroupListOut none{nullptr, nullptr, 0};
-        MR_TRY_CUDA(launch_pdl(csort_prefix_kernel, dim3(pblocks), dim3(kPrefixBuckets * kPrefixGroups),
-                               0, s, offs, nblk, (int)p.Eu, totals, bstart, ticket, none));
-        const int64_t work = items > p.n ? items : p.n;
-        MR_TRY_CUDA(launch_pdl(mask_scatter_kernel, dim3(elementwise_grid(work)), dim3(256), 0, s,
-                               (const uint32_t*)masks, (const uint32_t*)offs, (const uint32_t*)bstart,
-                               p.T, p.Eu, p.n, reinterpret_cast<const uint8_t*>(probs), p.pes, pp));
-    } else if (p.probs && p.padded) {
-        MR_TRY_CUDA(launch_pdl(padded_probs_kernel, dim3(elementwise_grid(p.n)), dim3(256), 0, s,
-                               sortedIndices, p.n, p.T, p.Eu, p.cap,
-                               reinterpret_cast<const uint8_t*>(probs), p.pes, pp));
-    }
+    // ---- permuteProbs (maskedSelect or the padded lookup) --------------------
+    auto launch_probs = [&](cudaStream_t ss) -> cudaError_t {
+        if (p.probs && !p.padded) {
+            const int64_t nblk = (p.T + 31) / 32;
+            const int64_t items = nblk * p.Eu;
+            uint8_t* q = wp;
+            uint32_t* masks = reinterpret_cast<uint32_t*>(q);
+            q += align_up((uint64_t)items * 4u, 256);
+            uint32_t* offs = reinterpret_cast<uint32_t*>(q);
+            q += align_up((uint64_t)items * 4u, 256);
+            uint32_t* totals = reinterpret_cast<uint32_t*>(q);
+            q += align_up((uint64_t)p.Eu * 4u, 256);
+            uint32_t* bstart = reinterpret_cast<uint32_t*>(q);
+            q += align_up((uint64_t)(p.Eu + 1) * 4u, 256);
+            uint32_t* ticket = reinterpret_cast<uint32_t*>(q);
+            cudaError_t e = launch_pdl(mask_columns_kernel, dim3(elementwise_grid(nblk * 32)),
+                                       dim3(256), 0, ss, routingMap, p.T, p.Eu, masks, offs, ticket);
+            if (e != cudaSuccess) return e;
+            GroupListOut none{nullptr, nullptr, 0};
+            e = csort_prefix(offs, nblk, (int)p.Eu, totals, bstart, ticket, none, ss);
+            if (e != cudaSuccess) return e;
+            const int64_t work = p.T * p.Eu > p.n ? p.T * p.Eu : p.n;
+            return launch_pdl(mask_scatter_kernel, dim3(elementwise_grid(work)), dim3(256), 0, ss,
+                              routingMap, (const uint32_t*)masks, (const uint32_t*)offs,
+                              (const uint32_t*)bstart, p.T, p.Eu, p.n,
+                              reinterpret_cast<const uint8_t*>(probs), p.pes, pp);
+        }
+        if (p.probs && p.padded) {
+            return launch_pdl(padded_probs_kernel, dim3(elementwise_grid(p.n)), dim3(256), 0, ss,
+                              sortedIndices, p.n, p.T, p.Eu, p.cap,
+                              reinterpret_cast<const uint8_t*>(probs), p.pes, pp);
+        }
+        return cudaSuccess;
+    };
 
     // ---- stable sort of sortedIndices -> outIndex, permuteTokenId ----------
     uint8_t* q = wp + p.ms_bytes;
@@ -663,55 +722,90 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
     q += align_up((uint64_t)p.n * 4u, 256);
     int32_t* ptr = p.padded ? reinterpret_cast<int32_t*>(q) : nullptr;
 
-    const int64_t limit = p.padded ? p.T : p.rows;
-    const uint32_t* kin = nullptr;
-    const int32_t* iin = nullptr;
-    for (int pass = 0; pass < p.passes; ++pass) {
-        const int B = p.passes == 1 ? (int)p.key_range : (1 << p.bits[pass]);
-        const uint32_t mask = p.passes == 1 ? 0xffffffffu : (uint32_t)((1u << p.bits[pass]) - 1u);
-        RadixKey kf{sortedIndices, kin, limit, p.padded ? 1 : 0, p.shift[pass], mask};
-        GroupListOut none{nullptr, nullptr, 0};
-        MR_TRY_CUDA(csort_run(kf, p.n, B, cs, none, s));
-        const bool last = pass == p.passes - 1;
-        MR_TRY_CUDA(launch_pdl(radix_scatter_kernel, dim3(elementwise_grid(p.n)), dim3(256), 0, s, kf,
-                               p.n, B, cs, iin, keys[pass & 1], last ? nullptr : idx[pass & 1],
-                               last ? outIndex : nullptr, last ? permuteTokenId : nullptr,
-                               p.topk > 0 ? p.topk : (int64_t)1));
-        kin = keys[pass & 1];
-        iin = idx[pass & 1];
-    }
-    if (p.padded) {
-        MR_TRY_CUDA(launch_pdl(csr_from_keys_kernel, dim3(elementwise_grid(p.n + 1)), dim3(256), 0, s,
-                               kin, p.n, p.T, ptr));
-    }
-    profile_mark(s, 5);
+    auto launch_sort = [&](cudaStream_t ss) -> cudaError_t {
+        const int64_t limit = p.padded ? p.T : p.rows;
+        const uint32_t* kin = nullptr;
+        const int32_t* iin = nullptr;
+        for (int pass = 0; pass < p.passes; ++pass) {
+            const int B = p.passes == 1 ? (int)p.key_range : (1 << p.bits[pass]);
+            const uint32_t mask =
+                p.passes == 1 ? 0xffffffffu : (uint32_t)((1u << p.bits[pass]) - 1u);
+            RadixKey kf{sortedIndices, kin, limit, p.padded ? 1 : 0, p.shift[pass], mask};
+            GroupListOut none{nullptr, nullptr, 0};
+            cudaError_t e = csort_run(kf, p.n, B, cs, none, ss);
+            if (e != cudaSuccess) return e;
+            const bool last = pass == p.passes - 1;
+            e = launch_pdl(radix_scatter_kernel, dim3(elementwise_grid(p.n)), dim3(256), 0, ss, kf,
+                           p.n, B, cs, iin, keys[pass & 1], last ? nullptr : idx[pass & 1],
+                           last ? outIndex : nullptr, last ? permuteTokenId : nullptr,
+                           p.topk > 0 ? p.topk : (int64_t)1);
+            if (e != cudaSuccess) return e;
+            kin = keys[pass & 1];
+            iin = idx[pass & 1];
+        }
+        if (p.padded) {
+            return launch_pdl(csr_from_keys_kernel, dim3(elementwise_grid(p.n + 1)), dim3(256), 0,
+                              ss, kin, p.n, p.T, ptr);
+        }
+        return cudaSuccess;
+    };
 
     // ---- gather-reduce --------------------------------------------------------
-    profile_mark(s, 6);
     const uint8_t* permuted = reinterpret_cast<const uint8_t*>(permutedTokens);
     uint8_t* out = reinterpret_cast<uint8_t*>(unpermutedTokens);
+    auto launch_reduce_any = [&](cudaStream_t ss) -> cudaError_t {
+        switch (p.tdt * 4 + p.pdt) {
+            case MR_DTYPE_F16 * 4 + MR_DTYPE_F16:
+                return dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss);
+            case MR_DTYPE_F16 * 4 + MR_DTYPE_F32:
+                return dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss);
+            case MR_DTYPE_BF16 * 4 + MR_DTYPE_BF16:
+                return dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_BF16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss);
+            case MR_DTYPE_BF16 * 4 + MR_DTYPE_F32:
+                return dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss);
+            case MR_DTYPE_F32 * 4 + MR_DTYPE_F32:
+                return dispatch_reduce<MR_DTYPE_F32, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss);
+        }
+        return cudaErrorInvalidValue;
+    };
+
     cudaError_t e = cudaSuccess;
-    switch (p.tdt * 4 + p.pdt) {
-        case MR_DTYPE_F16 * 4 + MR_DTYPE_F16:
-            e = dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, s);
-            break;
-        case MR_DTYPE_F16 * 4 + MR_DTYPE_F32:
-            e = dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, s);
-            break;
-        case MR_DTYPE_BF16 * 4 + MR_DTYPE_BF16:
-            e = dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_BF16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, s);
-            break;
-        case MR_DTYPE_BF16 * 4 + MR_DTYPE_F32:
-            e = dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, s);
-            break;
-        case MR_DTYPE_F32 * 4 + MR_DTYPE_F32:
-            e = dispatch_reduce<MR_DTYPE_F32, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, s);
-            break;
-        default:
-            return MR_ERR_PARAM_INVALID;
+    if (!p.padded) {
+        // Not padded, the sort's outputs are not read by the gather-reduce: it
+        // runs on the library's auxiliary stream, forked from and joined back
+        // into the caller's stream, so it overlaps the reduce.
+        AuxStream* ax = aux_stream();
+        if (!ax) return MR_ERR_CUDA;
+        std::lock_guard<std::mutex> lock(ax->mu);
+        MR_TRY_CUDA(cudaEventRecord(ax->fork, s));
+        MR_TRY_CUDA(cudaStreamWaitEvent(ax->stream, ax->fork, 0));
+        profile_mark(ax->stream, 8);
+        e = launch_sort(ax->stream);
+        profile_mark(ax->stream, 9);
+        const cudaError_t ej = cudaEventRecord(ax->join, ax->stream);
+        if (e == cudaSuccess) {
+            profile_mark(s, 4);
+            e = launch_probs(s);
+            profile_mark(s, 5);
+        }
+        if (e == cudaSuccess) {
+            profile_mark(s, 6);
+            e = launch_reduce_any(s);
+            profile_mark(s, 7);
+        }
+        const cudaError_t ew = ej == cudaSuccess ? cudaStreamWaitEvent(s, ax->join, 0) : ej;
+        MR_TRY_CUDA(e);
+        MR_TRY_CUDA(ew);
+    } else {
+        profile_mark(s, 4);
+        MR_TRY_CUDA(launch_probs(s));
+        MR_TRY_CUDA(launch_sort(s));
+        profile_mark(s, 5);
+        profile_mark(s, 6);
+        e = launch_reduce_any(s);
+        MR_TRY_CUDA(e);
+        profile_mark(s, 7);
     }
-    MR_TRY_CUDA(e);
-    profile_mark(s, 7);
     MR_TRY_CUDA(cudaGetLastError());
     return MR_OK;
 }
