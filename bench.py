@@ -55,6 +55,10 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-sample-attn", type=int, default=32,
                     help="attention workers (A) of the oracle's bounded sample (full workload: 256)")
     ap.add_argument("--small", action="store_true", help="a small case of the same workload (profiling)")
+    ap.add_argument("--workload", choices=["roundtrip", "tiny", "topk", "int8", "padded"],
+                    default="roundtrip",
+                    help="roundtrip (the bench line) or one of the other workloads, timed per call "
+                         "with an L2 flush before each")
     return ap.parse_args(argv)
 
 
@@ -486,10 +490,110 @@ def run_ours(args):
     return 0
 
 
+# ---------------------------------------------------------------------------
+# The other workloads (supplementary timing, one call per iteration)
+# ---------------------------------------------------------------------------
+
+def run_workload(args):
+    """Time one operation on one of the other workloads: each iteration
+    flushes L2 (a 512 MB write) and is timed alone with CUDA events."""
+    import torch
+
+    import unpermute_stable_counting_gb300 as usc
+    from unpermute_stable_counting_gb300 import _build
+    _build.build_library()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    name = args.workload
+    if name in ("tiny", "int8"):
+        spec = dict(w.BATCHING_TINY if name == "tiny" else w.BATCHING_INT8_DECODE)
+        inp = w.make_batching(**spec)
+        Y, H, E, dt = inp["Y"], inp["H"], inp["expertNum"], inp["tokenDtype"]
+        El = E // max(inp["layerNum"], 1)
+        U = int(((inp["expert_ids"] >= 0) & (inp["expert_ids"] < El)).sum())
+        s = 1 if dt == w.DT_INT8 else 2
+        sc = 4 if dt == w.DT_INT8 else 0
+        alg = (Y * 4 + U * (H * s + sc) + U * 12) + (U * (H * s + sc) + Y * 16 + E * 16 + 8)
+        units, unit_name = U, "slots"
+        args_d = dict(ids=g(inp["expert_ids"]), td=g(inp["token_data"]), sess=g(inp["session_in"]),
+                      micro=g(inp["micro_in"]), tok=g(inp["token_in"]))
+        shape = (inp["A"], inp["BS"], inp["K1"], H)
+        out = usc.batching_outputs(Y, H, E, dt, dev)
+        ws = torch.empty(usc.batching_workspace_size(E, shape, dt, inp["layerNum"]), dtype=torch.uint8,
+                         device=dev)
+
+        def call():
+            usc.ffnwb_batching(args_d["ids"], args_d["td"], args_d["sess"], args_d["micro"], expert_num=E,
+                               max_out_shape=shape, token_dtype=dt, layer_num=inp["layerNum"],
+                               layer_id=inp["layer_id"], token_ids=args_d["tok"],
+                               token_row_stride=inp["row_stride"], out=out, workspace=ws)
+        phases = (0, 1)
+    else:
+        if name == "topk":
+            u = w.make_unpermute_topk(**w.UNPERMUTE_TOPK)
+        else:
+            u = w.make_unpermute_padded(**w.UNPERMUTE_PADDED)
+        T, H, n, dt, pdt, Eu = u["T"], u["H"], u["n"], u["tokenDtype"], u["probsDtype"], u["Eu"]
+        s, ps = w.ELEM_BYTES[dt], w.ELEM_BYTES[pdt]
+        si = u["sortedIndices"].astype(np.int64)
+        if u["padded"]:
+            V = int(((si >= 0) & (si < T)).sum())
+            alg = n * (4 + H * s + ps) + T * H * s + n * (8 + ps)
+        else:
+            pr = u["probs"].reshape(T, Eu)
+            pv = pr.T[(u["routingMap"] != 0).T]
+            wgt = np.zeros(n, bool)
+            wgt[:min(n, pv.size)] = pv[:n] != 0
+            V = int((((si >= 0) & (si < u["permutedRows"])) & wgt).sum())
+            alg = n * 4 + V * H * s + T * Eu * (1 + ps) + T * H * s + n * (8 + ps)
+        units, unit_name = T, "tokens"
+        tdt = {0: torch.float16, 1: torch.bfloat16, 3: torch.float32}
+        fl = lambda a, d: (g(a) if d == 3 else g(np.ascontiguousarray(a).view(np.int16)).view(tdt[d]))
+        perm, sidx, rm, pr_d = fl(u["permuted"], dt), g(u["sortedIndices"]), g(u["routingMap"]), fl(u["probs"], pdt)
+        out = usc.unpermute_outputs(T, H, n, dt, pdt, dev)
+        ws = torch.empty(usc.unpermute_workspace_size(u["permutedRows"], H, dt, n, True, pdt, T, Eu,
+                                                      bool(u["padded"])), dtype=torch.uint8, device=dev)
+
+        def call():
+            usc.moe_unpermute(perm, sidx, rm, pr_d, padded_mode=bool(u["padded"]), out=out, workspace=ws)
+        phases = (2, 3)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
+    for _ in range(max(args.warmup, 3)):
+        call()
+    torch.cuda.synchronize()
+    usc.profile_set_events(ev)
+    tot, ph = [], {p: [] for p in phases}
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    try:
+        for _ in range(args.steps):
+            flush.fill_(1)
+            e0.record()
+            call()
+            e1.record()
+            torch.cuda.synchronize()
+            tot.append(e0.elapsed_time(e1) / 1e3)
+            for p in phases:
+                ph[p].append(ev[2 * p].elapsed_time(ev[2 * p + 1]) / 1e3)
+    finally:
+        usc.profile_set_events(None)
+    sec = statistics.median(tot)
+    peak, _ = hbm_peak()
+    line = {"workload": name, "value": alg / sec / 1e9, "unit": "GB/s", "us_per_call": sec * 1e6,
+            "frac_of_hbm_peak": alg / sec / 1e9 / peak, f"{unit_name}_per_s": units / sec,
+            "alg_bytes": alg, "phase_us": {str(p): statistics.median(v) * 1e6 for p, v in ph.items()},
+            "l2": "flushed before every call (512 MB write)"}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.workload != "roundtrip":
+        return run_workload(args)
     return run_ours(args)
 
 

@@ -138,3 +138,22 @@ def test_tail_rows_untouched():
     assert U < inp["Y"]
     tail = out["y"][U:].float()
     assert bool((tail == 7.0).all())
+
+
+@pytest.mark.parametrize("H", [16, 48, 4112, 7168])
+def test_int8_rows_with_interleaved_scale_shift_path(H):
+    """INT8 rows of stride H + 4 start at 4-byte offsets 0, 4, 8, 12: the
+    16-byte windows path (H a multiple of 16) and its last-vector tail."""
+    inp = w.make_batching(A=2, BS=16, K1=9, E=64, H=H, dtype=2, ids="zipf", mask=0.1, seed=H)
+    check(inp)
+
+
+def test_int8_rows_unaligned_buffer_base():
+    """A token buffer whose base is not 16-byte aligned takes the word path."""
+    inp = w.make_batching(A=2, BS=16, K1=9, E=64, H=64, dtype=2, ids="zipf", mask=0.1, seed=5)
+    raw = inp["token_data"].reshape(-1)
+    buf = torch.zeros(raw.size + 16, dtype=torch.uint8, device="cuda:0")
+    buf[4:4 + raw.size] = torch.from_numpy(raw).to("cuda:0")
+    view = buf[4:4 + raw.size].view(inp["Y"], -1)
+    assert view.data_ptr() % 16 == 4
+    check(inp, token_data=view)

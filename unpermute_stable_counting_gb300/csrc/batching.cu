@@ -63,6 +63,65 @@ batching_scatter_kernel(BatchKey kf, int64_t Y, int B, CsortBufs cs,
     }
 }
 
+// 16-byte output vectors from a source that is only 4-byte aligned (INT8 rows
+// with their trailing scale have a stride of H + 4 bytes). With o = src % 16
+// (4, 8 or 12) and `win` the aligned address src - o, output vector j is the
+// tail of window j followed by the head of window j + 1. Lane l loads window
+// j = j0 + l and takes window j + 1 from lane l + 1 by a shuffle. Windows up to
+// nvec - 1 lie inside [win, src + bytes); the last output vector is read as
+// words. The caller uses this only when the buffer base is 16-byte aligned,
+// so win never precedes the buffer.
+constexpr int kShiftVPT = 4;
+
+__device__ __forceinline__ uint4 shift_combine(const uint4& a, const uint4& b, int o) {
+    if (o == 4) return make_uint4(a.y, a.z, a.w, b.x);
+    if (o == 8) return make_uint4(a.z, a.w, b.x, b.y);
+    return make_uint4(a.w, b.x, b.y, b.z);
+}
+
+__device__ __forceinline__ void warp_copy_row_shift(const uint8_t* __restrict__ src,
+                                                    uint8_t* __restrict__ dst, int64_t bytes,
+                                                    int lane) {
+    const int o = (int)(reinterpret_cast<uintptr_t>(src) & 15u);
+    const uint4* win = reinterpret_cast<const uint4*>(src - o);
+    const int nv1 = (int)(bytes >> 4) - 1;  // vectors built from two windows
+    for (int j0 = 0; j0 < nv1; j0 += 32 * kShiftVPT) {
+        uint4 a[kShiftVPT];
+#pragma unroll
+        for (int u = 0; u < kShiftVPT; ++u) {
+            const int j = j0 + 32 * u + lane;
+            a[u] = j <= nv1 ? ld_stream_v4(win + j) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        // lane 31's next window: lane 0's window of the next u, or one more load
+        const int jl = j0 + 32 * (kShiftVPT - 1) + 31;
+        const uint4 extra = (lane == 31 && jl < nv1) ? ld_stream_v4(win + jl + 1)
+                                                     : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int u = 0; u < kShiftVPT; ++u) {
+            const int j = j0 + 32 * u + lane;
+            uint4 b;
+            b.x = __shfl_down_sync(0xffffffffu, a[u].x, 1);
+            b.y = __shfl_down_sync(0xffffffffu, a[u].y, 1);
+            b.z = __shfl_down_sync(0xffffffffu, a[u].z, 1);
+            b.w = __shfl_down_sync(0xffffffffu, a[u].w, 1);
+            if (u + 1 < kShiftVPT) {
+                const uint4 nx = make_uint4(__shfl_sync(0xffffffffu, a[u + 1 < kShiftVPT ? u + 1 : u].x, 0),
+                                            __shfl_sync(0xffffffffu, a[u + 1 < kShiftVPT ? u + 1 : u].y, 0),
+                                            __shfl_sync(0xffffffffu, a[u + 1 < kShiftVPT ? u + 1 : u].z, 0),
+                                            __shfl_sync(0xffffffffu, a[u + 1 < kShiftVPT ? u + 1 : u].w, 0));
+                if (lane == 31) b = nx;
+            } else if (lane == 31) {
+                b = extra;
+            }
+            if (j < nv1) st_stream_v4(dst + 16 * (int64_t)j, shift_combine(a[u], b, o));
+        }
+    }
+    if (lane == 0 && nv1 >= 0) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(src + 16 * (int64_t)nv1);
+        st_stream_v4(dst + 16 * (int64_t)nv1, make_uint4(w[0], w[1], w[2], w[3]));
+    }
+}
+
 // Copy `bytes` from src to dst with one warp. Vector width follows the common
 // alignment of both addresses and the length: 16-byte vectors (VPT in flight
 // per lane), else 4-byte words, else bytes. Addresses are formed from the
@@ -71,7 +130,8 @@ batching_scatter_kernel(BatchKey kf, int64_t Y, int B, CsortBufs cs,
 // against 626 us for the round-trip gather with pointer casts).
 template <int VPT>
 __device__ __forceinline__ void warp_copy_row(const uint8_t* __restrict__ src,
-                                              uint8_t* __restrict__ dst, int64_t bytes, int lane) {
+                                              uint8_t* __restrict__ dst, int64_t bytes, int lane,
+                                              bool base16) {
     const uintptr_t mis = (reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) |
                            (uintptr_t)bytes);
     if ((mis & 15u) == 0u) {
@@ -91,6 +151,9 @@ __device__ __forceinline__ void warp_copy_row(const uint8_t* __restrict__ src,
 #pragma unroll
         for (int u = 0; u < VPT; ++u)
             if (v + 32 * u < nv) st_stream_v4(dst + 16 * (v + 32 * u), r[u]);
+    } else if (base16 && ((reinterpret_cast<uintptr_t>(dst) | (uintptr_t)bytes) & 15u) == 0u &&
+               (reinterpret_cast<uintptr_t>(src) & 3u) == 0u) {
+        warp_copy_row_shift(src, dst, bytes, lane);
     } else if ((mis & 3u) == 0u) {
         constexpr int W = VPT * 4;
         const int64_t nw = bytes >> 2;
@@ -118,15 +181,20 @@ batching_gather_kernel(const uint8_t* __restrict__ token_data, int64_t row_strid
     pdl_enter();
     const uint32_t U = bucket_start[E];
     const int lane = threadIdx.x & 31;
+    const bool base16 = (reinterpret_cast<uintptr_t>(token_data) & 15u) == 0u;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t i = gw; i < (int64_t)U; i += nw) {
         const int64_t g = gather_idx[i];
-        warp_copy_row<VPT>(token_data + g * row_stride, y + i * row_bytes, row_bytes, lane);
-        if (is_int8 && lane < 4) {
-            // 4 scale bytes, one per lane (the scale is only 4-byte aligned at best)
+        warp_copy_row<VPT>(token_data + g * row_stride, y + i * row_bytes, row_bytes, lane, base16);
+        if (is_int8) {
             const uint8_t* sp = scales ? scales + g * scale_stride : token_data + g * row_stride + row_bytes;
-            reinterpret_cast<uint8_t*>(dyn + i)[lane] = sp[lane];
+            if ((reinterpret_cast<uintptr_t>(sp) & 3u) == 0u) {
+                if (lane == 0) dyn[i] = *reinterpret_cast<const float*>(sp);
+            } else if (lane < 4) {
+                // an unaligned scale: one byte per lane
+                reinterpret_cast<uint8_t*>(dyn + i)[lane] = sp[lane];
+            }
         }
     }
 }
