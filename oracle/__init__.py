@@ -69,6 +69,10 @@ def _load():
             _P, _I32, _P, _I64, _P, _I64, _P, _P, _P,
             _I64, _I64, _I64, _I64, _I64, _I64, _I64,
             _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+        lib.oracle_batching_context.restype = _I32
+        lib.oracle_batching_context.argtypes = [
+            _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
+            _P, _P, _P, _P, _P, _P, _P, _P, _P]
         lib.oracle_unpermute.restype = _I32
         lib.oracle_unpermute.argtypes = [
             _P, _P, _P, _P, _I64, _I64, _I32, _I64, _I32, _I64, _I64, _I32,
@@ -159,6 +163,32 @@ def batching(inp: dict, *, with_gather_idx: bool = False) -> dict:
     if with_gather_idx:
         out["gather_idx"] = gidx
     return out
+
+
+def batching_context(ctx: np.ndarray, token_info: np.ndarray, token_data: np.ndarray, *,
+                     expertNum: int, maxOutShape, tokenDtype: int, needSchedule: int,
+                     layerNum: int) -> dict:
+    """Run the ScheduleContext batching oracle. ctx: the 1024 context bytes;
+    token_info / token_data: host copies of the buffers the context points to."""
+    A, BS, K1, H = (int(v) for v in maxOutShape)
+    Y, E = A * BS * K1, int(expertNum)
+    row_bytes = H * ELEM_BYTES[tokenDtype]
+    y = np.zeros((Y, row_bytes), dtype=np.uint8)
+    gl = np.empty((E, 2), dtype=np.int64)
+    sess, micro, tok, eoff = (np.empty(Y, dtype=np.int32) for _ in range(4))
+    dyn = np.zeros(Y, dtype=np.float32) if tokenDtype == 2 else None
+    atn = np.zeros(1, dtype=np.int64)
+    status = np.zeros(1, dtype=np.int32)
+    rc = _load().oracle_batching_context(
+        _ptr(np.ascontiguousarray(ctx, dtype=np.uint8)), _ptr(np.ascontiguousarray(token_info)),
+        _ptr(np.ascontiguousarray(token_data)), E, A, BS, K1, H, int(tokenDtype), int(needSchedule),
+        int(layerNum), _ptr(y), _ptr(gl), _ptr(sess), _ptr(micro), _ptr(tok), _ptr(eoff), _ptr(dyn),
+        _ptr(atn), _ptr(status))
+    if rc != 0:
+        raise ValueError(f"oracle_batching_context rejected its arguments (code {rc})")
+    return dict(y=y, groupList=gl, sessionIds=sess, microBatchIds=micro, tokenIds=tok,
+                expertOffsets=eoff, dynamicScale=dyn, actualTokenNum=int(atn[0]),
+                status=int(status[0]))
 
 
 def unpermute(inp: dict) -> dict:

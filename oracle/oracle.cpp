@@ -296,6 +296,130 @@ int oracle_batching(const int32_t* expert_ids, int32_t layer_id, const uint8_t* 
 }
 
 // ---------------------------------------------------------------------------
+// FFN-worker batching from a ScheduleContext  [FWB 功能说明 step 1, the
+// ScheduleContext / FfnDataDesc structs and the token_info / token_data fill
+// of 调用示例]
+//
+// The 1024-byte packed context: CommonArea at byte 0 (u32 session_num,
+// micro_batch_num, micro_batch_size, selected_expert_num, expert_num, ...),
+// ControlArea at 128, AttentionArea at 256, FfnArea at 384 (u64
+// token_info_buf, token_info_buf_size, token_data_buf, token_data_buf_size,
+// ...). token_info_buf holds one FfnDataDesc per (session, micro-batch) block,
+// sessions outer: i32 flag, i32 layer_id, then micro_batch_size *
+// selected_expert_num i32 expert ids. token_data_buf holds one row per slot in
+// the same order.
+//
+// Readings:
+//  * The slots are the blocks' expert ids in block order; slot g of block b
+//    has session id b / micro_batch_num, micro-batch id b % micro_batch_num
+//    and token id g.
+//  * Each block carries its own layer_id: key = layer_id * E_l + id; a block
+//    whose layer_id is outside [0, max(layerNum,1)) has all its slots masked.
+//  * needSchedule = 1: a block takes part only if its flag is 1 (ready);
+//    otherwise all its slots are masked. needSchedule = 0 ignores the flags.
+//    `status` = number of blocks not ready (0 with needSchedule = 0).
+//  * The context is invalid when a count is 0, the context's slots exceed
+//    Y = A*BS*(topK+1) of maxOutShape, expert_num != E_l, or a buffer is
+//    NULL or too small: then every slot is masked and status = -1.
+//  * Outputs are sized for Y rows; rows past the context's slots belong to
+//    the masked tail (ids -1, y untouched).
+// The host copies of token_info_buf / token_data_buf are passed separately
+// (the context itself holds device addresses).
+// ---------------------------------------------------------------------------
+int oracle_batching_context(const uint8_t* ctx, const uint8_t* token_info,
+                            const uint8_t* token_data, int64_t expertNum, int64_t A, int64_t BS,
+                            int64_t K1, int64_t H, int64_t tokenDtype, int64_t needSchedule,
+                            int64_t layerNum, uint8_t* y, int64_t* group_list,
+                            int32_t* session_out, int32_t* micro_out, int32_t* token_out,
+                            int32_t* expert_offsets, float* dynamic_scale,
+                            int64_t* actual_token_num, int32_t* status) {
+    if (expertNum <= 0 || A <= 0 || BS <= 0 || K1 <= 0 || H <= 0) return 1;
+    const int64_t Y = A * BS * K1;
+    const int64_t E = expertNum;
+    const int64_t L = layerNum > 0 ? layerNum : 1;
+    if (E % L != 0) return 3;
+    const int64_t El = E / L;
+    const int64_t es = (int64_t)elem_bytes((int32_t)tokenDtype);
+    const int64_t row_bytes = H * es;
+    const int64_t row_stride = row_bytes + (tokenDtype == DT_INT8 ? 4 : 0);
+
+    uint32_t common[5];
+    std::memcpy(common, ctx, sizeof(common));
+    const int64_t sessions = common[0], micro = common[1], mbs = common[2], sel = common[3];
+    const int64_t expert_num_ctx = common[4];
+    uint64_t ffn[4];
+    std::memcpy(ffn, ctx + 384, sizeof(ffn));  // info buf, info size, data buf, data size
+    const int64_t per_block = mbs * sel;
+    const int64_t blocks = sessions * micro;
+    const int64_t slots = blocks * per_block;
+    const int64_t block_bytes = 8 + 4 * per_block;
+    bool valid = sessions > 0 && micro > 0 && mbs > 0 && sel > 0 && slots <= Y &&
+                 expert_num_ctx == El && ffn[0] != 0 && ffn[2] != 0 &&
+                 (int64_t)ffn[1] >= blocks * block_bytes && (int64_t)ffn[3] >= slots * row_stride;
+
+    std::vector<int64_t> key(Y, E);
+    std::vector<int32_t> sess(Y, 0), mb(Y, 0);
+    int32_t not_ready = 0;
+    if (valid) {
+        for (int64_t b = 0; b < blocks; ++b) {
+            const uint8_t* desc = token_info + b * block_bytes;
+            int32_t flag, layer;
+            std::memcpy(&flag, desc, 4);
+            std::memcpy(&layer, desc + 4, 4);
+            const bool ready = needSchedule == 0 || flag == 1;
+            if (!ready) ++not_ready;
+            for (int64_t j = 0; j < per_block; ++j) {
+                const int64_t g = b * per_block + j;
+                int32_t id;
+                std::memcpy(&id, desc + 8 + 4 * j, 4);
+                if (ready && layer >= 0 && layer < L && id >= 0 && id < El) key[g] = layer * El + id;
+                sess[g] = (int32_t)(b / micro);
+                mb[g] = (int32_t)(b % micro);
+            }
+        }
+    }
+    if (status) status[0] = valid ? not_ready : -1;
+
+    std::vector<int64_t> gather_idx(Y);
+    std::iota(gather_idx.begin(), gather_idx.end(), (int64_t)0);
+    std::stable_sort(gather_idx.begin(), gather_idx.end(),
+                     [&](int64_t a, int64_t b) { return key[a] < key[b]; });
+    int64_t U = 0;
+    for (int64_t s = 0; s < Y; ++s) U += key[s] < E ? 1 : 0;
+    for (int64_t i = 0; i < U; ++i) {
+        const int64_t g = gather_idx[i];
+        std::memcpy(y + i * row_bytes, token_data + g * row_stride, (size_t)row_bytes);
+        if (tokenDtype == DT_INT8) std::memcpy(&dynamic_scale[i], token_data + g * row_stride + row_bytes, 4);
+    }
+    int64_t group_start = 0;
+    for (int64_t i = 0; i < Y; ++i) {
+        const int64_t g = gather_idx[i];
+        if (i < U) {
+            if (i == 0 || key[gather_idx[i - 1]] != key[g]) group_start = i;
+            session_out[i] = sess[g];
+            micro_out[i] = mb[g];
+            token_out[i] = (int32_t)g;
+            expert_offsets[i] = (int32_t)(i - group_start);
+        } else {
+            session_out[i] = micro_out[i] = token_out[i] = expert_offsets[i] = -1;
+        }
+    }
+    int64_t rows = 0;
+    for (int64_t i = 0; i < U; ++i) {
+        const int64_t k = key[gather_idx[i]];
+        if (i == 0 || key[gather_idx[i - 1]] != k) {
+            group_list[2 * rows] = k;
+            group_list[2 * rows + 1] = 0;
+            ++rows;
+        }
+        group_list[2 * (rows - 1) + 1] += 1;
+    }
+    for (int64_t r = rows; r < E; ++r) group_list[2 * r] = group_list[2 * r + 1] = 0;
+    actual_token_num[0] = U;
+    return 0;
+}
+
+// ---------------------------------------------------------------------------
 // Routing-map unpermute  [UNP 功能说明与计算公式 branches (1)-(4)]
 //
 // Derived sizes: topK_num = permutedRows // numTokens, capacity =

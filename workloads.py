@@ -257,3 +257,40 @@ ROUNDTRIP_BATCHING = dict(A=256, BS=64, K1=9, E=1024, H=7168, dtype=DT_BF16, lay
                           layer_id=2, ids="zipf", zipf_s=1.2, mask=0.05, session=256, micro=64,
                           token_ids=True, seed=4)
 ROUNDTRIP_PROBS_DTYPE = DT_BF16
+
+
+# ---------------------------------------------------------------------------
+# ScheduleContext inputs ("aclnnFfnWorkerBatching", 调用示例: the packed
+# 1024-byte ScheduleContext and the FfnArea token_info / token_data buffers)
+# ---------------------------------------------------------------------------
+
+CTX_BYTES = 1024
+CTX_FFN_OFFSET = 384  # CommonArea 128 + ControlArea 128 + AttentionArea 128
+
+
+def make_token_info(*, sessions: int, micro: int, mbs: int, sel: int, expert_ids: np.ndarray,
+                    layer_ids, flags) -> np.ndarray:
+    """token_info_buf bytes: per (session, micro-batch) block, sessions outer,
+    i32 flag, i32 layer_id, then mbs*sel i32 expert ids (FfnDataDesc)."""
+    blocks = sessions * micro
+    per = mbs * sel
+    ids = np.asarray(expert_ids, dtype=np.int32).reshape(blocks, per)
+    out = np.empty((blocks, 2 + per), dtype=np.int32)
+    out[:, 0] = np.broadcast_to(np.asarray(flags, dtype=np.int32), (blocks,))
+    out[:, 1] = np.broadcast_to(np.asarray(layer_ids, dtype=np.int32), (blocks,))
+    out[:, 2:] = ids
+    return out.view(np.uint8).reshape(-1)
+
+
+def pack_schedule_context(*, sessions: int, micro: int, mbs: int, sel: int, expert_num: int,
+                          info_ptr: int, info_size: int, data_ptr: int, data_size: int,
+                          run_flag: int = 1) -> np.ndarray:
+    """The packed ScheduleContext (1024 bytes) with the CommonArea counts and
+    the FfnArea token_info / token_data buffer addresses and sizes."""
+    ctx = np.zeros(CTX_BYTES, dtype=np.uint8)
+    common = np.array([sessions, micro, mbs, sel, expert_num, 0, 0, 0], dtype=np.uint32)
+    ctx[0:32] = common.view(np.uint8)
+    ctx[128:132] = np.array([run_flag], dtype=np.int32).view(np.uint8)
+    ffn = np.array([info_ptr, info_size, data_ptr, data_size], dtype=np.uint64)
+    ctx[CTX_FFN_OFFSET:CTX_FFN_OFFSET + 32] = ffn.view(np.uint8)
+    return ctx
