@@ -150,6 +150,53 @@ mr_status ffnwb_batching(const int32_t* expertIds, int32_t layerId, const void* 
                          uint64_t workspaceSize, void* stream);
 
 /*
+ * ffnwb_batching_context_get_workspace_size / ffnwb_batching_context
+ *   "aclnnFfnWorkerBatching", 功能说明 step 1 (read the FFN side's data area),
+ *   参数说明 (scheduleContext, needSchedule) and the ScheduleContext /
+ *   FfnDataDesc structs of 调用示例: the batching of ffnwb_batching with the
+ *   page's own input, a packed 1024-byte ScheduleContext in device memory.
+ *
+ *   scheduleContext  device pointer, 8-byte aligned, 1024 bytes: CommonArea at
+ *                    0 (u32 session_num, micro_batch_num, micro_batch_size,
+ *                    selected_expert_num, expert_num = experts per layer),
+ *                    FfnArea at 384 (u64 token_info_buf, token_info_buf_size,
+ *                    token_data_buf, token_data_buf_size; device addresses).
+ *                    token_info_buf holds one block per (session, micro-batch),
+ *                    sessions outer: i32 flag, i32 layer_id, then
+ *                    micro_batch_size * selected_expert_num i32 expert ids.
+ *                    token_data_buf holds one row per slot in the same order:
+ *                    H values (FP16/BF16) or H int8 values and their fp32
+ *                    scale (INT8, stride H + 4).
+ *   Slot g of block b: session id b / micro_batch_num, micro-batch id
+ *   b % micro_batch_num, token id g, key = layer_id(b) * E_l + id (masked if
+ *   the id or the block's layer is out of range).
+ *   needSchedule     0: use every block. 1: a block takes part only once its
+ *                    flag reads 1; the kernel waits for each flag until
+ *                    waitTimeoutUs (at most 60 s) after it starts, and masks
+ *                    the blocks still not ready.
+ *   scheduleStatus   int32 [1], nullable device output: the number of blocks
+ *                    that were not ready, or -1 if the context does not fit
+ *                    (a count is 0, the slots exceed Y = A*BS*(topK+1) of
+ *                    maxOutShape, expert_num != E_l, or a buffer is NULL,
+ *                    misaligned or too small); then every slot is masked.
+ *   The other arguments and the outputs are those of ffnwb_batching (outputs
+ *   sized for Y rows; rows past the context's slots are part of the masked
+ *   tail). The context is read on the device; nothing is synchronised.
+ *   Returns the codes of ffnwb_batching.
+ */
+mr_status ffnwb_batching_context_get_workspace_size(int64_t expertNum, const int64_t* maxOutShape,
+                                                    int64_t tokenDtype, int64_t needSchedule,
+                                                    int64_t layerNum, uint64_t* workspaceSize);
+mr_status ffnwb_batching_context(const void* scheduleContext, int64_t expertNum,
+                                 const int64_t* maxOutShape, int64_t tokenDtype,
+                                 int64_t needSchedule, int64_t layerNum, int64_t waitTimeoutUs,
+                                 void* y, int64_t* groupList, int32_t* sessionIds,
+                                 int32_t* microBatchIds, int32_t* tokenIds, int32_t* expertOffsets,
+                                 float* dynamicScale, int64_t* actualTokenNum,
+                                 int32_t* scheduleStatus, void* workspace, uint64_t workspaceSize,
+                                 void* stream);
+
+/*
  * ffnwb_batching_noalloc -- the batching for callers that cannot allocate.
  *   No counterpart on the pages: the pages' two-stage calls always take a
  *   caller-allocated workspace. Some callers cannot allocate device memory

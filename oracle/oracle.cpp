@@ -320,7 +320,8 @@ int oracle_batching(const int32_t* expert_ids, int32_t layer_id, const uint8_t* 
 //    `status` = number of blocks not ready (0 with needSchedule = 0).
 //  * The context is invalid when a count is 0, the context's slots exceed
 //    Y = A*BS*(topK+1) of maxOutShape, expert_num != E_l, or a buffer is
-//    NULL or too small: then every slot is masked and status = -1.
+//    NULL or too small, or token_info_buf is not 4-byte aligned (its fields
+//    are int32): then every slot is masked and status = -1.
 //  * Outputs are sized for Y rows; rows past the context's slots belong to
 //    the masked tail (ids -1, y untouched).
 // The host copies of token_info_buf / token_data_buf are passed separately
@@ -354,7 +355,7 @@ int oracle_batching_context(const uint8_t* ctx, const uint8_t* token_info,
     const int64_t slots = blocks * per_block;
     const int64_t block_bytes = 8 + 4 * per_block;
     bool valid = sessions > 0 && micro > 0 && mbs > 0 && sel > 0 && slots <= Y &&
-                 expert_num_ctx == El && ffn[0] != 0 && ffn[2] != 0 &&
+                 expert_num_ctx == El && ffn[0] != 0 && ffn[2] != 0 && (ffn[0] & 3u) == 0 &&
                  (int64_t)ffn[1] >= blocks * block_bytes && (int64_t)ffn[3] >= slots * row_stride;
 
     std::vector<int64_t> key(Y, E);

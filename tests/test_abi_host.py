@@ -202,3 +202,42 @@ def test_profile_events_validation(L):
     assert L.mr_profile_set_events(None, 2) == INVALID
     assert L.mr_profile_set_events(None, 17) == INVALID
     assert L.mr_profile_set_events(None, -1) == INVALID
+
+
+def _context_call(L, **kw):
+    a = dict(ctx=ctypes.c_void_p(0x1000), E=8, shape=(2, 8, 3, 128), dt=0, ns=0, ln=1, timeout=1000,
+             y=FAKE, gl=FAKE, so=FAKE, mo=FAKE, to=FAKE, eo=FAKE, dyn=None, atn=FAKE, status=None,
+             ws=FAKE, wsz=1 << 40, stream=None)
+    a.update(kw)
+    return L.ffnwb_batching_context(a["ctx"], a["E"], _native.int64_array(a["shape"]), a["dt"], a["ns"],
+                                    a["ln"], a["timeout"], a["y"], a["gl"], a["so"], a["mo"], a["to"],
+                                    a["eo"], a["dyn"], a["atn"], a["status"], a["ws"], a["wsz"],
+                                    a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(ctx=None), NULLPTR),
+    (dict(y=None), NULLPTR),
+    (dict(atn=None), NULLPTR),
+    (dict(ws=None), NULLPTR),
+    (dict(dt=2, dyn=None), NULLPTR),
+    (dict(ctx=ctypes.c_void_p(0x1004)), INVALID),      # not 8-byte aligned
+    (dict(timeout=-1), INVALID),
+    (dict(timeout=60_000_001), INVALID),
+    (dict(ns=2), INVALID),
+    (dict(E=0), INVALID),
+    (dict(wsz=8), WORKSPACE),
+])
+def test_context_execute_validation(L, kw, expect):
+    assert _context_call(L, **kw) == expect
+
+
+def test_context_workspace_size(L):
+    ws = ctypes.c_uint64(0)
+    shape = _native.int64_array((2, 8, 3, 128))
+    assert L.ffnwb_batching_context_get_workspace_size(8, shape, 0, 1, 1, ctypes.byref(ws)) == OK
+    ws_flat = ctypes.c_uint64(0)
+    assert L.ffnwb_batching_get_workspace_size(8, shape, 0, 0, 1, ctypes.byref(ws_flat)) == OK
+    assert ws.value > ws_flat.value
+    assert L.ffnwb_batching_context_get_workspace_size(8, shape, 0, 2, 1, ctypes.byref(ws)) == INVALID
+    assert L.ffnwb_batching_context_get_workspace_size(8, shape, 0, 0, 1, None) == NULLPTR

@@ -57,8 +57,8 @@ def test_page_example_through_the_context(need):
     info = w.make_token_info(sessions=1, micro=1, mbs=8, sel=9, expert_ids=np.arange(Y) % 8,
                              layer_ids=0, flags=1)
     data = np.full((Y, p["H"]), 1, dtype=np.uint16).view(np.uint8).reshape(-1)
-    ctx = w.pack_schedule_context(sessions=1, micro=1, mbs=8, sel=9, expert_num=8, info_ptr=1,
-                                  info_size=info.size, data_ptr=2, data_size=data.size)
+    ctx = w.pack_schedule_context(sessions=1, micro=1, mbs=8, sel=9, expert_num=8, info_ptr=0x1000,
+                                  info_size=info.size, data_ptr=0x2000, data_size=data.size)
     o = run(ctx, info, data, (p["A"], p["BS"], p["K1"], p["H"]), 8, 0, need)
     assert o["status"] == 0
     assert o["groupList"].tolist() == [[e, 9] for e in range(8)]
@@ -128,7 +128,7 @@ def test_unready_blocks_are_masked_with_need_schedule():
 
 
 @pytest.mark.parametrize("bad", ["too_many_slots", "expert_num", "null_data", "small_info", "small_data",
-                                 "zero_sessions"])
+                                 "zero_sessions", "misaligned_info"])
 def test_invalid_context_masks_everything(bad):
     ids = np.zeros(8, np.int32)
     kw = dict(sessions=2, micro=1, mbs=2, sel=2, E=2, H=8, dtype=1, ids=ids)
@@ -145,6 +145,8 @@ def test_invalid_context_masks_everything(bad):
     ctx, info, data, shape, _ = build(**kw)
     if bad == "zero_sessions":
         ctx[0:4] = 0
+    if bad == "misaligned_info":
+        ctx[384:392] = np.array([0x1002], np.uint64).view(np.uint8)
     o = run(ctx, info, data, shape, 2, 1, 0)
     assert o["status"] == -1 and o["actualTokenNum"] == 0
     assert np.all(o["tokenIds"] == -1) and np.all(o["groupList"] == 0)

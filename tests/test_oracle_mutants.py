@@ -1,8 +1,9 @@
 """The pins catch plausible mistakes.
 
 Each case plants one mistake in a temporary copy of the oracle source (never
-in the committed oracle), builds it on the CPU, and runs the pin suite against
-that library. The suite must fail for every mutant.
+in the committed oracle; every occurrence of the anchor text is changed),
+builds it on the CPU, and runs the pin suites against that library. The
+suites must fail for every mutant.
 """
 import os
 import subprocess
@@ -78,6 +79,15 @@ MUTANTS = [
     ("accumulate_descending",
      "for (int64_t i = 0; i < n; ++i) {\n            const int64_t v = sortedIndices[i];\n            if (v < 0 || v >= permutedRows) continue;",
      "for (int64_t i = n - 1; i >= 0; --i) {\n            const int64_t v = sortedIndices[i];\n            if (v < 0 || v >= permutedRows) continue;"),
+    ("context_session_micro_swapped",
+     "sess[g] = (int32_t)(b / micro);",
+     "sess[g] = (int32_t)(b % micro);"),
+    ("context_flag_ignored",
+     "const bool ready = needSchedule == 0 || flag == 1;",
+     "const bool ready = true;"),
+    ("context_block_layer_ignored",
+     "key[g] = layer * El + id;",
+     "key[g] = id;"),
     ("double_weighting",
      "if (has_probs) term = x * p;\n                acc[(size_t)(t * H + h)] = acc[(size_t)(t * H + h)] + term;\n            }\n        }\n    } else {",
      "if (has_probs) term = (x * p) * p;\n                acc[(size_t)(t * H + h)] = acc[(size_t)(t * H + h)] + term;\n            }\n        }\n    } else {"),
@@ -87,12 +97,13 @@ MUTANTS = [
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_pins_catch_mutant(name, old, new, tmp_path):
     src = open(SRC).read()
-    assert src.count(old) == 1, f"mutant {name}: anchor text not found exactly once"
+    assert src.count(old) >= 1, f"mutant {name}: anchor text not found"
     mutant_src = tmp_path / "oracle_mutant.cpp"
     mutant_src.write_text(src.replace(old, new))
     lib = oracle.compile_library(str(mutant_src), str(tmp_path / "liboracle_mutant.so"))
     env = dict(os.environ, USC_ORACLE_LIB=lib)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(HERE, "test_oracle_pins.py")],
+                        os.path.join(HERE, "test_oracle_pins.py"),
+                        os.path.join(HERE, "test_oracle_context_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"

@@ -12,10 +12,11 @@ CUDA kernels for sm_103a:
 Importing the package does not load the CUDA library; the first call does,
 and fails loudly if the library was not built.
 """
-from .api import (DT_BF16, DT_F16, DT_F32, DT_INT8, MoeReorderError, batching_outputs,
-                  batching_workspace_size, ffnwb_batching, moe_unpermute, profile_set_events,
-                  unpermute_outputs, unpermute_workspace_size)
+from .api import (DT_BF16, DT_F16, DT_F32, DT_INT8, MoeReorderError, batching_context_workspace_size,
+                  batching_outputs, batching_workspace_size, ffnwb_batching, ffnwb_batching_context,
+                  moe_unpermute, profile_set_events, unpermute_outputs, unpermute_workspace_size)
 
-__all__ = ["ffnwb_batching", "moe_unpermute", "batching_workspace_size",
+__all__ = ["ffnwb_batching", "ffnwb_batching_context", "moe_unpermute",
+           "batching_context_workspace_size", "batching_workspace_size",
            "unpermute_workspace_size", "batching_outputs", "unpermute_outputs",
            "profile_set_events", "MoeReorderError", "DT_F16", "DT_BF16", "DT_INT8", "DT_F32"]

@@ -22,6 +22,9 @@ SIGNATURES = {
     "ffnwb_batching_get_workspace_size": (_I32, [_I64, _PI64, _I64, _I64, _I64, _PU64]),
     "ffnwb_batching": (_I32, [_P, _I32, _P, _I64, _P, _I64, _P, _P, _P, _I64, _PI64, _I64, _I64,
                               _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _U64, _P]),
+    "ffnwb_batching_context_get_workspace_size": (_I32, [_I64, _PI64, _I64, _I64, _I64, _PU64]),
+    "ffnwb_batching_context": (_I32, [_P, _I64, _PI64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P,
+                                      _P, _P, _P, _P, _P, _U64, _P]),
     "ffnwb_batching_noalloc": (_I32, [_P, _I32, _P, _I64, _P, _I64, _P, _P, _P, _I64, _PI64, _I64,
                                       _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_unpermute_get_workspace_size": (_I32, [_I64, _I64, _I32, _I64, _I32, _I32, _I64, _I64,

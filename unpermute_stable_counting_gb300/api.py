@@ -123,6 +123,46 @@ def ffnwb_batching(expert_ids, token_data, session_ids, micro_batch_ids, *, expe
     return out
 
 
+def batching_context_workspace_size(expert_num: int, max_out_shape, token_dtype: int,
+                                    layer_num: int, need_schedule: int = 0) -> int:
+    ws = ctypes.c_uint64(0)
+    _check(lib().ffnwb_batching_context_get_workspace_size(
+        expert_num, int64_array(max_out_shape), token_dtype, need_schedule, layer_num,
+        ctypes.byref(ws)), "ffnwb_batching_context_get_workspace_size")
+    return int(ws.value)
+
+
+def ffnwb_batching_context(schedule_context, *, expert_num: int, max_out_shape, token_dtype: int,
+                           layer_num: int = 1, need_schedule: int = 0,
+                           wait_timeout_us: int = 1_000_000, out: dict | None = None,
+                           workspace=None, stream=None) -> dict:
+    """Batching from a ScheduleContext (a CUDA tensor of its 1024 bytes) on the
+    current stream. Returns the batching outputs plus scheduleStatus (int32 [1]):
+    blocks not ready with need_schedule = 1, or -1 for a context that does not fit."""
+    _require_cuda("schedule_context", schedule_context)
+    if schedule_context.numel() * schedule_context.element_size() < 1024:
+        raise ValueError("schedule_context must hold 1024 bytes")
+    A, BS, K1, H = (int(v) for v in max_out_shape)
+    dev = schedule_context.device
+    if out is None:
+        out = batching_outputs(A * BS * K1, H, expert_num, token_dtype, dev)
+    if out.get("scheduleStatus") is None:
+        out["scheduleStatus"] = torch.zeros(1, dtype=torch.int32, device=dev)
+    if workspace is None:
+        ws = batching_context_workspace_size(expert_num, max_out_shape, token_dtype, layer_num,
+                                             need_schedule)
+        workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+    st = lib().ffnwb_batching_context(
+        _ptr(schedule_context), int(expert_num), int64_array(max_out_shape), int(token_dtype),
+        int(need_schedule), int(layer_num), int(wait_timeout_us), _ptr(out["y"]),
+        _ptr(out["groupList"]), _ptr(out["sessionIds"]), _ptr(out["microBatchIds"]),
+        _ptr(out["tokenIds"]), _ptr(out["expertOffsets"]), _ptr(out.get("dynamicScale")),
+        _ptr(out["actualTokenNum"]), _ptr(out["scheduleStatus"]), _ptr(workspace),
+        int(workspace.numel()), _stream(stream, dev))
+    _check(st, "ffnwb_batching_context")
+    return out
+
+
 # ---------------------------------------------------------------------------
 # Routing-map unpermute
 # ---------------------------------------------------------------------------
