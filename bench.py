@@ -55,7 +55,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-sample-attn", type=int, default=32,
                     help="attention workers (A) of the oracle's bounded sample (full workload: 256)")
     ap.add_argument("--small", action="store_true", help="a small case of the same workload (profiling)")
-    ap.add_argument("--workload", choices=["roundtrip", "tiny", "topk", "int8", "padded"],
+    ap.add_argument("--workload", choices=["roundtrip", "tiny", "topk", "int8", "padded", "context",
+                                           "batching"],
                     default="roundtrip",
                     help="roundtrip (the bench line) or one of the other workloads, timed per call "
                          "with an L2 flush before each")
@@ -507,7 +508,47 @@ def run_workload(args):
     g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     name = args.workload
-    if name in ("tiny", "int8"):
+    if name in ("context", "batching"):
+        # the round trip's batching alone, from flat arrays or from a
+        # ScheduleContext (256 sessions x 4 micro-batches x 16 tokens x 9)
+        spec = dict(w.ROUNDTRIP_BATCHING)
+        inp = w.make_batching(**spec)
+        Y, H, E, dt = inp["Y"], inp["H"], inp["expertNum"], inp["tokenDtype"]
+        El = E // max(inp["layerNum"], 1)
+        U = int(((inp["expert_ids"] >= 0) & (inp["expert_ids"] < El)).sum())
+        row = H * 2
+        alg = (Y * 4 + U * row + U * 12) + (U * row + Y * 16 + E * 16 + 8)
+        units, unit_name = U, "slots"
+        shape = (inp["A"], inp["BS"], inp["K1"], H)
+        out = usc.batching_outputs(Y, H, E, dt, dev)
+        td = g(inp["token_data"])
+        if name == "context":
+            info = w.make_token_info(sessions=256, micro=4, mbs=16, sel=9, expert_ids=inp["expert_ids"],
+                                     layer_ids=inp["layer_id"], flags=1)
+            info_d = g(info)
+            ctx = w.pack_schedule_context(sessions=256, micro=4, mbs=16, sel=9, expert_num=El,
+                                          info_ptr=info_d.data_ptr(), info_size=info.size,
+                                          data_ptr=td.data_ptr(), data_size=td.numel())
+            ctx_d = g(ctx)
+            ws = torch.empty(usc.batching_context_workspace_size(E, shape, dt, inp["layerNum"], 1),
+                             dtype=torch.uint8, device=dev)
+
+            def call():
+                usc.ffnwb_batching_context(ctx_d, expert_num=E, max_out_shape=shape, token_dtype=dt,
+                                           layer_num=inp["layerNum"], need_schedule=1, out=out,
+                                           workspace=ws)
+        else:
+            ids, sess, micro = g(inp["expert_ids"]), g(inp["session_in"]), g(inp["micro_in"])
+            tok = g(inp["token_in"])
+            ws = torch.empty(usc.batching_workspace_size(E, shape, dt, inp["layerNum"]), dtype=torch.uint8,
+                             device=dev)
+
+            def call():
+                usc.ffnwb_batching(ids, td, sess, micro, expert_num=E, max_out_shape=shape, token_dtype=dt,
+                                   layer_num=inp["layerNum"], layer_id=inp["layer_id"], token_ids=tok,
+                                   out=out, workspace=ws)
+        phases = (0, 1)
+    elif name in ("tiny", "int8"):
         spec = dict(w.BATCHING_TINY if name == "tiny" else w.BATCHING_INT8_DECODE)
         inp = w.make_batching(**spec)
         Y, H, E, dt = inp["Y"], inp["H"], inp["expertNum"], inp["tokenDtype"]
