@@ -73,6 +73,8 @@ def _load():
         lib.oracle_batching_context.argtypes = [
             _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
             _P, _P, _P, _P, _P, _P, _P, _P, _P]
+        lib.oracle_permute.restype = _I32
+        lib.oracle_permute.argtypes = [_P, _P, _I64, _I64, _I32, _I64, _I64, _I32, _I64, _P, _P, _P]
         lib.oracle_unpermute.restype = _I32
         lib.oracle_unpermute.argtypes = [
             _P, _P, _P, _P, _I64, _I64, _I32, _I64, _I32, _I64, _I64, _I32,
@@ -189,6 +191,26 @@ def batching_context(ctx: np.ndarray, token_info: np.ndarray, token_data: np.nda
     return dict(y=y, groupList=gl, sessionIds=sess, microBatchIds=micro, tokenIds=tok,
                 expertOffsets=eoff, dynamicScale=dyn, actualTokenNum=int(atn[0]),
                 status=int(status[0]))
+
+
+def permute(tokens: np.ndarray, routing_map: np.ndarray, *, tokenDtype: int, topK: int = 0,
+            padded: int = 0, capacity: int = 0) -> dict:
+    """Run the permute oracle. tokens: storage [T, H] (uint16 bits or float32);
+    routing_map: int8/bool [T, Eu]. Returns permuted (storage [rows, H]),
+    sortedIndices and rows (rows written, not padded / kept, padded)."""
+    T, H = tokens.shape
+    Eu = routing_map.shape[1]
+    rows = Eu * capacity if padded else T * topK
+    permuted = np.zeros((rows, H), dtype=tokens.dtype)
+    si = np.empty(rows, dtype=np.int32)
+    rows_out = np.zeros(1, dtype=np.int32)
+    rc = _load().oracle_permute(
+        _ptr(np.ascontiguousarray(tokens)), _ptr(np.ascontiguousarray(routing_map).view(np.int8)), T, H,
+        int(tokenDtype), Eu, int(topK), int(padded), int(capacity), _ptr(permuted), _ptr(si),
+        _ptr(rows_out))
+    if rc != 0:
+        raise ValueError(f"oracle_permute rejected its arguments (code {rc})")
+    return dict(permuted=permuted, sortedIndices=si, rows=int(rows_out[0]))
 
 
 def unpermute(inp: dict) -> dict:

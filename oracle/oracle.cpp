@@ -421,6 +421,79 @@ int oracle_batching_context(const uint8_t* ctx, const uint8_t* token_info,
 }
 
 // ---------------------------------------------------------------------------
+// Routing-map permute  [UNP 算子定位: the permute step that precedes the
+// unpermute rearranges the tokens by routingMap into an expert-grouped compact
+// layout, permutedTokens, so that each expert reads its tokens contiguously]
+//
+// Readings, chosen so that the unpermute takes these outputs:
+//  * Not padded: the rows are the (token, expert) pairs with routingMap = 1 in
+//    expert-major order (expert ascending, then token ascending): the order of
+//    probs.T.maskedSelect(routingMap.T). permutedTokens[r] = tokens[t(r)] for
+//    r < topK*T. sortedIndices[t*topK + j] = row of t's j-th routed expert
+//    (ascending expert id), -1 for j >= its count; a pair whose row is not
+//    below topK*T gets -1 too. rows_out = min(pairs, topK*T).
+//  * Padded (capacity layout): expert e keeps its first `capacity` routed
+//    tokens (ascending token id) in rows e*capacity + r; sortedIndices of those
+//    rows = the token id; the remaining rows are padding: sortedIndices -1 and
+//    a zero row. rows_out = rows kept.
+// ---------------------------------------------------------------------------
+int oracle_permute(const void* tokens, const int8_t* routingMap, int64_t T, int64_t H,
+                   int32_t tokenDtype, int64_t Eu, int64_t topK, int32_t padded, int64_t capacity,
+                   void* permuted, int32_t* sortedIndices, int32_t* rows_out) {
+    if (T <= 0 || H <= 0 || Eu <= 0) return 1;
+    const size_t row_bytes = (size_t)H * elem_bytes(tokenDtype);
+    const uint8_t* src = (const uint8_t*)tokens;
+    uint8_t* dst = (uint8_t*)permuted;
+    if (!padded) {
+        if (topK <= 0) return 2;
+        const int64_t n = T * topK;
+        // rows in expert-major order
+        std::vector<int64_t> row_of((size_t)(T * Eu), -1);
+        int64_t r = 0;
+        for (int64_t e = 0; e < Eu; ++e) {
+            for (int64_t t = 0; t < T; ++t) {
+                if (routingMap[t * Eu + e] != 0) {
+                    row_of[(size_t)(t * Eu + e)] = r;
+                    if (r < n) std::memcpy(dst + (size_t)r * row_bytes, src + (size_t)t * row_bytes, row_bytes);
+                    ++r;
+                }
+            }
+        }
+        for (int64_t t = 0; t < T; ++t) {
+            int64_t j = 0;
+            for (int64_t e = 0; e < Eu; ++e) {
+                const int64_t ro = row_of[(size_t)(t * Eu + e)];
+                if (ro < 0) continue;
+                if (j < topK) sortedIndices[t * topK + j] = ro < n ? (int32_t)ro : -1;
+                ++j;
+            }
+            for (; j < topK; ++j) sortedIndices[t * topK + j] = -1;
+        }
+        rows_out[0] = (int32_t)(r < n ? r : n);
+    } else {
+        if (capacity <= 0) return 3;
+        int64_t kept = 0;
+        for (int64_t e = 0; e < Eu; ++e) {
+            int64_t r = 0;
+            for (int64_t t = 0; t < T; ++t) {
+                if (routingMap[t * Eu + e] != 0 && r < capacity) {
+                    sortedIndices[e * capacity + r] = (int32_t)t;
+                    std::memcpy(dst + (size_t)(e * capacity + r) * row_bytes, src + (size_t)t * row_bytes, row_bytes);
+                    ++r;
+                }
+            }
+            kept += r;
+            for (; r < capacity; ++r) {
+                sortedIndices[e * capacity + r] = -1;
+                std::memset(dst + (size_t)(e * capacity + r) * row_bytes, 0, row_bytes);
+            }
+        }
+        rows_out[0] = (int32_t)kept;
+    }
+    return 0;
+}
+
+// ---------------------------------------------------------------------------
 // Routing-map unpermute  [UNP 功能说明与计算公式 branches (1)-(4)]
 //
 // Derived sizes: topK_num = permutedRows // numTokens, capacity =

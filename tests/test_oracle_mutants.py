@@ -88,6 +88,15 @@ MUTANTS = [
     ("context_block_layer_ignored",
      "key[g] = layer * El + id;",
      "key[g] = id;"),
+    ("permute_copies_wrong_row",
+     "if (r < n) std::memcpy(dst + (size_t)r * row_bytes, src + (size_t)t * row_bytes, row_bytes);",
+     "if (r < n) std::memcpy(dst + (size_t)r * row_bytes, src + (size_t)(r % T) * row_bytes, row_bytes);"),
+    ("permute_slot_off_by_one",
+     "if (j < topK) sortedIndices[t * topK + j] = ro < n ? (int32_t)ro : -1;",
+     "if (j < topK) sortedIndices[t * topK + j] = ro < n ? (int32_t)ro + 1 : -1;"),
+    ("permute_pad_not_minus_one",
+     "sortedIndices[e * capacity + r] = -1;",
+     "sortedIndices[e * capacity + r] = 0;"),
     ("double_weighting",
      "if (has_probs) term = x * p;\n                acc[(size_t)(t * H + h)] = acc[(size_t)(t * H + h)] + term;\n            }\n        }\n    } else {",
      "if (has_probs) term = (x * p) * p;\n                acc[(size_t)(t * H + h)] = acc[(size_t)(t * H + h)] + term;\n            }\n        }\n    } else {"),
@@ -104,6 +113,7 @@ def test_pins_catch_mutant(name, old, new, tmp_path):
     env = dict(os.environ, USC_ORACLE_LIB=lib)
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(HERE, "test_oracle_pins.py"),
-                        os.path.join(HERE, "test_oracle_context_pins.py")],
+                        os.path.join(HERE, "test_oracle_context_pins.py"),
+                        os.path.join(HERE, "test_oracle_permute_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
