@@ -56,7 +56,7 @@ def parse_args(argv=None):
                     help="attention workers (A) of the oracle's bounded sample (full workload: 256)")
     ap.add_argument("--small", action="store_true", help="a small case of the same workload (profiling)")
     ap.add_argument("--workload", choices=["roundtrip", "tiny", "topk", "int8", "padded", "context",
-                                           "batching"],
+                                           "batching", "permute", "permute_padded"],
                     default="roundtrip",
                     help="roundtrip (the bench line) or one of the other workloads, timed per call "
                          "with an L2 flush before each")
@@ -508,7 +508,34 @@ def run_workload(args):
     g = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     name = args.workload
-    if name in ("context", "batching"):
+    if name in ("permute", "permute_padded"):
+        # the permute that produces the top-k / padded unpermute inputs
+        if name == "permute":
+            u = w.make_unpermute_topk(**w.UNPERMUTE_TOPK)
+            kw = dict(topk=u["n"] // u["T"])
+        else:
+            u = w.make_unpermute_padded(**w.UNPERMUTE_PADDED)
+            kw = dict(padded_mode=True, capacity=u["n"] // u["Eu"])
+        T, H, dt, Eu = u["T"], u["H"], u["tokenDtype"], u["Eu"]
+        s = w.ELEM_BYTES[dt]
+        x = w.normal_rows(T, H, dt, seed=5)
+        tdt = {0: torch.float16, 1: torch.bfloat16, 3: torch.float32}
+        xd = g(x.view(np.int16)).view(tdt[dt]) if dt != 3 else g(x)
+        md = g(u["routingMap"])
+        pairs = int(u["routingMap"].astype(np.int64).sum())
+        rows = u["n"] if name == "permute_padded" else pairs
+        alg = T * Eu + T * H * s + rows * H * s + u["n"] * 4
+        units, unit_name = T, "tokens"
+        ws = torch.empty(usc.permute_workspace_size(T, H, dt, Eu, kw.get("topk", 0),
+                                                    kw.get("padded_mode", False), kw.get("capacity", 0)),
+                         dtype=torch.uint8, device=dev)
+        out = None
+
+        def call():
+            nonlocal out
+            out = usc.moe_permute(xd, md, out=out, workspace=ws, **kw)
+        phases = (0, 1)
+    elif name in ("context", "batching"):
         # the round trip's batching alone, from flat arrays or from a
         # ScheduleContext (256 sessions x 4 micro-batches x 16 tokens x 9)
         spec = dict(w.ROUNDTRIP_BATCHING)

@@ -306,6 +306,44 @@ mr_status moe_unpermute(const void* permutedTokens, const int32_t* sortedIndices
                         int32_t* outIndex, int32_t* permuteTokenId, void* permuteProbs,
                         void* workspace, uint64_t workspaceSize, void* stream);
 
+/*
+ * moe_permute_get_workspace_size / moe_permute
+ *   "MoeTokenUnpermuteWithRoutingMap 算子全解析", 算子定位: the permute step
+ *   that precedes the unpermute rearranges the tokens by routingMap into an
+ *   expert-grouped compact layout (permutedTokens), so each expert reads its
+ *   tokens contiguously. The page names this step without its formulas; the
+ *   layouts below are the ones moe_unpermute takes.
+ *
+ *   tokens          [numTokens, hidden] of tokenDtype (F16, BF16 or F32).
+ *   routingMap      int8/bool [numTokens, numExperts]; numExperts in [1, 8192].
+ *   paddedMode 0    topK in [1, 512] slots per token (561103 above 512).
+ *                   permutedTokens [numTokens*topK, hidden]: the routed
+ *                   (token, expert) pairs in expert-major order (expert, then
+ *                   token ascending) -- the order of probs.T.maskedSelect(
+ *                   routingMap.T); rows past the pairs are not written.
+ *                   sortedIndices int32 [numTokens*topK]: slot t*topK + j =
+ *                   row of t's j-th routed expert (ascending id), -1 for j at
+ *                   or past its count and for a pair whose row would be past
+ *                   numTokens*topK.
+ *   paddedMode 1    capacity >= 1. permutedTokens [numExperts*capacity,
+ *                   hidden]: expert e keeps its first `capacity` routed tokens
+ *                   (ascending token id) in rows e*capacity + r; the other
+ *                   rows are zero. sortedIndices int32 [numExperts*capacity]:
+ *                   the row's token id, -1 for a padding row.
+ *   permutedRowsOut int32 [1], nullable: rows written from tokens (not
+ *                   padded: min(pairs, numTokens*topK); padded: rows kept).
+ *   Returns MR_OK, MR_ERR_PARAM_NULLPTR, MR_ERR_PARAM_INVALID, MR_ERR_INNER,
+ *   MR_ERR_WORKSPACE or MR_ERR_CUDA.
+ */
+mr_status moe_permute_get_workspace_size(int64_t numTokens, int64_t hidden, int32_t tokenDtype,
+                                         int64_t numExperts, int64_t topK, int32_t paddedMode,
+                                         int64_t capacity, uint64_t* workspaceSize);
+mr_status moe_permute(const void* tokens, const int8_t* routingMap, int64_t numTokens,
+                      int64_t hidden, int32_t tokenDtype, int64_t numExperts, int64_t topK,
+                      int32_t paddedMode, int64_t capacity, void* permutedTokens,
+                      int32_t* sortedIndices, int32_t* permutedRowsOut, void* workspace,
+                      uint64_t workspaceSize, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Utilities (no counterpart on the pages)                                  */
 /* ------------------------------------------------------------------------ */

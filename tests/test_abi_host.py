@@ -241,3 +241,39 @@ def test_context_workspace_size(L):
     assert ws.value > ws_flat.value
     assert L.ffnwb_batching_context_get_workspace_size(8, shape, 0, 2, 1, ctypes.byref(ws)) == INVALID
     assert L.ffnwb_batching_context_get_workspace_size(8, shape, 0, 0, 1, None) == NULLPTR
+
+
+def _permute_call(L, **kw):
+    a = dict(tok=FAKE, rmap=FAKE, T=16, H=32, dt=1, Eu=8, k=2, padded=0, cap=0, out=FAKE, si=FAKE,
+             rows=None, ws=FAKE, wsz=1 << 40, stream=None)
+    a.update(kw)
+    return L.moe_permute(a["tok"], a["rmap"], a["T"], a["H"], a["dt"], a["Eu"], a["k"], a["padded"],
+                         a["cap"], a["out"], a["si"], a["rows"], a["ws"], a["wsz"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(tok=None), NULLPTR),
+    (dict(rmap=None), NULLPTR),
+    (dict(out=None), NULLPTR),
+    (dict(si=None), NULLPTR),
+    (dict(ws=None), NULLPTR),
+    (dict(dt=2), INVALID),                 # int8 tokens
+    (dict(Eu=0), INVALID),
+    (dict(Eu=8193), INVALID),
+    (dict(k=0), INVALID),
+    (dict(k=513), INNER),                  # topK_num > 512
+    (dict(padded=1, cap=0), INVALID),
+    (dict(padded=2), INVALID),
+    (dict(T=0), INVALID),
+    (dict(wsz=8), WORKSPACE),
+])
+def test_permute_execute_validation(L, kw, expect):
+    assert _permute_call(L, **kw) == expect
+
+
+def test_permute_workspace_size(L):
+    ws = ctypes.c_uint64(0)
+    assert L.moe_permute_get_workspace_size(4096, 4096, 1, 64, 8, 0, 0, ctypes.byref(ws)) == OK
+    assert ws.value > 0
+    assert L.moe_permute_get_workspace_size(16384, 4096, 0, 128, 0, 1, 512, ctypes.byref(ws)) == OK
+    assert L.moe_permute_get_workspace_size(16, 32, 1, 8, 2, 0, 0, None) == NULLPTR

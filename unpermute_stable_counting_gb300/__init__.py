@@ -14,9 +14,11 @@ and fails loudly if the library was not built.
 """
 from .api import (DT_BF16, DT_F16, DT_F32, DT_INT8, MoeReorderError, batching_context_workspace_size,
                   batching_outputs, batching_workspace_size, ffnwb_batching, ffnwb_batching_context,
-                  moe_unpermute, profile_set_events, unpermute_outputs, unpermute_workspace_size)
+                  moe_permute, moe_unpermute, permute_workspace_size, profile_set_events,
+                  unpermute_outputs, unpermute_workspace_size)
 
-__all__ = ["ffnwb_batching", "ffnwb_batching_context", "moe_unpermute",
+__all__ = ["ffnwb_batching", "ffnwb_batching_context", "moe_unpermute", "moe_permute",
+           "permute_workspace_size",
            "batching_context_workspace_size", "batching_workspace_size",
            "unpermute_workspace_size", "batching_outputs", "unpermute_outputs",
            "profile_set_events", "MoeReorderError", "DT_F16", "DT_BF16", "DT_INT8", "DT_F32"]

@@ -235,6 +235,43 @@ def moe_unpermute(permuted_tokens, sorted_indices, routing_map=None, probs=None,
     return out
 
 
+def permute_workspace_size(T: int, H: int, token_dtype: int, Eu: int, topk: int = 0,
+                           padded_mode: bool = False, capacity: int = 0) -> int:
+    ws = ctypes.c_uint64(0)
+    _check(lib().moe_permute_get_workspace_size(T, H, token_dtype, Eu, topk, int(padded_mode),
+                                                capacity, ctypes.byref(ws)),
+           "moe_permute_get_workspace_size")
+    return int(ws.value)
+
+
+def moe_permute(tokens, routing_map, *, topk: int = 0, padded_mode: bool = False, capacity: int = 0,
+                out: dict | None = None, workspace=None, stream=None) -> dict:
+    """Permute tokens [T, H] by routing_map [T, Eu] on the current stream.
+    Returns permutedTokens, sortedIndices and permutedRows (int32 [1])."""
+    _require_cuda("tokens", tokens)
+    _require_cuda("routing_map", routing_map, (torch.int8, torch.bool, torch.uint8))
+    tdt = _TORCH_TO_DT.get(tokens.dtype)
+    if tdt is None:
+        raise TypeError(f"tokens dtype {tokens.dtype} is not f16/bf16/f32")
+    T, H = int(tokens.shape[0]), int(tokens.shape[1])
+    Eu = int(routing_map.shape[1])
+    rows = Eu * capacity if padded_mode else T * topk
+    dev = tokens.device
+    if out is None:
+        out = dict(permutedTokens=torch.empty((rows, H), dtype=tokens.dtype, device=dev),
+                   sortedIndices=torch.empty(rows, dtype=torch.int32, device=dev),
+                   permutedRows=torch.zeros(1, dtype=torch.int32, device=dev))
+    if workspace is None:
+        ws = permute_workspace_size(T, H, tdt, Eu, topk, padded_mode, capacity)
+        workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
+    st = lib().moe_permute(_ptr(tokens), _ptr(routing_map), T, H, tdt, Eu, int(topk),
+                           int(bool(padded_mode)), int(capacity), _ptr(out["permutedTokens"]),
+                           _ptr(out["sortedIndices"]), _ptr(out.get("permutedRows")),
+                           _ptr(workspace), int(workspace.numel()), _stream(stream, dev))
+    _check(st, "moe_permute")
+    return out
+
+
 def profile_set_events(events) -> None:
     """Attach cudaEvents (torch.cuda.Event, created with enable_timing) to the
     library's phase markers for this thread; None to detach."""

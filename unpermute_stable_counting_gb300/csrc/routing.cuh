@@ -1,0 +1,58 @@
+// Routing-map column masks, shared by the unpermute (maskedSelect) and the
+// permute: both order the routed (token, expert) pairs expert-major.
+#pragma once
+
+#include "csort.cuh"
+
+namespace mr {
+
+// ---------------------------------------------------------------------------
+// maskedSelect of probs.T by routingMap.T (not padded, with probs).
+// The routing map is cut into blocks of 32 tokens; item (blk, e) holds the
+// 32-bit mask of the block's tokens routed to expert e (built by one lane per
+// expert, reading 32 routing-map bytes). Its popcount is the
+// histogram entry of the counting sort whose key is the expert, so the
+// engine's prefix kernel turns them into positions: the j-th token of the
+// mask lands at bucket_start[e] + tile_off[blk][e] + (set bits below j).
+// ---------------------------------------------------------------------------
+static __global__ void __launch_bounds__(256)
+mask_columns_kernel(const int8_t* __restrict__ map, int64_t T, int64_t Eu,
+                    uint32_t* __restrict__ masks, uint32_t* __restrict__ counts,
+                    uint32_t* __restrict__ ticket) {
+    pdl_enter();
+    if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
+    // one warp per (32-token block, 32-expert chunk); lane = expert: 32
+    // coalesced loads of consecutive routing-map bytes, one per token
+    const int lane = threadIdx.x & 31;
+    const int64_t nblk = (T + 31) / 32;
+    const int64_t chunks = (Eu + 31) / 32;
+    const int64_t units = nblk * chunks;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t unit = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; unit < units;
+         unit += nwarps) {
+        const int64_t blk = unit / chunks;
+        const int64_t e = (unit - blk * chunks) * 32 + lane;
+        const int64_t t0 = blk * 32;
+        uint32_t bits = 0u;
+        if (e < Eu) {
+            int8_t m[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) m[j] = t0 + j < T ? map[(t0 + j) * Eu + e] : (int8_t)0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) bits |= (m[j] != 0 ? 1u : 0u) << j;
+            masks[blk * Eu + e] = bits;
+            counts[blk * Eu + e] = __popc(bits);
+        }
+    }
+}
+
+// Rank of token t among the tokens routed to expert e, from the block masks
+// and the per-block offsets the prefix kernel left in `offs`.
+__device__ __forceinline__ int64_t column_rank(const uint32_t* __restrict__ masks,
+                                               const uint32_t* __restrict__ offs, int64_t Eu,
+                                               int64_t t, int64_t e) {
+    const int64_t item = (t >> 5) * Eu + e;
+    return (int64_t)offs[item] + __popc(masks[item] & ((1u << (t & 31)) - 1u));
+}
+
+}  // namespace mr

@@ -20,7 +20,7 @@
 #include <cstdlib>
 #include <mutex>
 
-#include "csort.cuh"
+#include "routing.cuh"
 
 namespace mr {
 
@@ -31,44 +31,6 @@ __device__ __forceinline__ float ld_f32(const void* base, int64_t i) {
     } else {
         const uint16_t b = __ldg(reinterpret_cast<const unsigned short*>(base) + i);
         return Elem<DT>::to_f32(b);
-    }
-}
-
-// ---------------------------------------------------------------------------
-// maskedSelect of probs.T by routingMap.T (not padded, with probs).
-// The routing map is cut into blocks of 32 tokens; item (blk, e) holds the
-// 32-bit mask of the block's tokens routed to expert e. Its popcount is the
-// histogram entry of the counting sort whose key is the expert, so the
-// engine's prefix kernel turns them into positions: the j-th token of the
-// mask lands at bucket_start[e] + tile_off[blk][e] + (set bits below j).
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
-mask_columns_kernel(const int8_t* __restrict__ map, int64_t T, int64_t Eu,
-                    uint32_t* __restrict__ masks, uint32_t* __restrict__ counts,
-                    uint32_t* __restrict__ ticket) {
-    pdl_enter();
-    if (blockIdx.x == 0 && threadIdx.x == 0) *ticket = 0u;
-    // one warp per 32-token block; lane j reads token t0+j; a ballot per expert
-    const int lane = threadIdx.x & 31;
-    const int64_t nblk = (T + 31) / 32;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t blk = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; blk < nblk;
-         blk += nwarps) {
-        const int64_t t = blk * 32 + lane;
-        const int8_t* row = map + t * Eu;
-        for (int64_t e0 = 0; e0 < Eu; e0 += 8) {
-            int8_t m[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) m[u] = (t < T && e0 + u < Eu) ? row[e0 + u] : (int8_t)0;
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const uint32_t bits = __ballot_sync(0xffffffffu, m[u] != 0);
-                if (lane == u && e0 + u < Eu) {
-                    masks[blk * Eu + e0 + u] = bits;
-                    counts[blk * Eu + e0 + u] = __popc(bits);
-                }
-            }
-        }
     }
 }
 
@@ -686,7 +648,8 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
             uint32_t* bstart = reinterpret_cast<uint32_t*>(q);
             q += align_up((uint64_t)(p.Eu + 1) * 4u, 256);
             uint32_t* ticket = reinterpret_cast<uint32_t*>(q);
-            cudaError_t e = launch_pdl(mask_columns_kernel, dim3(elementwise_grid(nblk * 32)),
+            cudaError_t e = launch_pdl(mask_columns_kernel,
+                                       dim3(elementwise_grid(nblk * ((p.Eu + 31) / 32) * 32)),
                                        dim3(256), 0, ss, routingMap, p.T, p.Eu, masks, offs, ticket);
             if (e != cudaSuccess) return e;
             GroupListOut none{nullptr, nullptr, 0};
