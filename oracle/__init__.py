@@ -75,6 +75,9 @@ def _load():
             _P, _P, _P, _P, _P, _P, _P, _P, _P]
         lib.oracle_permute.restype = _I32
         lib.oracle_permute.argtypes = [_P, _P, _I64, _I64, _I32, _I64, _I64, _I32, _I64, _P, _P, _P]
+        lib.oracle_update_expert.restype = _I32
+        lib.oracle_update_expert.argtypes = [_P, _I32, _P, _P, _I32, _P, _P, _I64, _I64, _I64, _I64,
+                                             _I64, _I64, _P, _P]
         lib.oracle_unpermute.restype = _I32
         lib.oracle_unpermute.argtypes = [
             _P, _P, _P, _P, _I64, _I64, _I32, _I64, _I32, _I64, _I64, _I32,
@@ -211,6 +214,28 @@ def permute(tokens: np.ndarray, routing_map: np.ndarray, *, tokenDtype: int, top
     if rc != 0:
         raise ValueError(f"oracle_permute rejected its arguments (code {rc})")
     return dict(permuted=permuted, sortedIndices=si, rows=int(rows_out[0]))
+
+
+def update_expert(expert_ids: np.ndarray, table: np.ndarray, *, local_rank: int, balance_mode: int,
+                  scales: np.ndarray | None = None, scales_dtype: int = 3,
+                  threshold: np.ndarray | None = None, active: np.ndarray | None = None) -> dict:
+    """Run the MoeUpdateExpert oracle. expert_ids [BS, K] int32/int64; table
+    [moeExpertNum, F] int32; scales storage [BS, K]; threshold float32 [K];
+    active bool [BS]. Returns balancedExpertIds and balancedActiveMask (or None)."""
+    ids = np.ascontiguousarray(expert_ids)
+    BS, K = ids.shape
+    E, F = table.shape
+    out = np.empty_like(ids)
+    mask = np.zeros((BS, K), np.uint8) if (scales is not None and threshold is not None) else None
+    rc = _load().oracle_update_expert(
+        _ptr(ids), ids.dtype.itemsize, _ptr(np.ascontiguousarray(table, dtype=np.int32)),
+        _ptr(None if scales is None else np.ascontiguousarray(scales)), int(scales_dtype),
+        _ptr(None if threshold is None else np.ascontiguousarray(threshold, dtype=np.float32)),
+        _ptr(None if active is None else np.ascontiguousarray(active).astype(np.uint8)),
+        BS, K, E, F, int(local_rank), int(balance_mode), _ptr(out), _ptr(mask))
+    if rc != 0:
+        raise ValueError(f"oracle_update_expert rejected its arguments (code {rc})")
+    return dict(balancedExpertIds=out, balancedActiveMask=None if mask is None else mask.astype(bool))
 
 
 def unpermute(inp: dict) -> dict:

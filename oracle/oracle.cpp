@@ -15,6 +15,8 @@
 //          参数说明 / 补充说明 (shapes and ranges), Kernel 实现 (pad kernel
 //          prob lookup, IsValidInputIndex, prob != 0 skip, fp32 Cast/Muls/Add,
 //          CAST_RINT).
+//   [UPD]  "MoeUpdateExpert" (CANN ops-transformer README): 功能说明,
+//          参数说明 and 约束说明.
 //
 // Readings where the pages are silent or garbled are listed in the design doc and
 // restated at each use below.
@@ -489,6 +491,66 @@ int oracle_permute(const void* tokens, const int8_t* routingMap, int64_t T, int6
             }
         }
         rows_out[0] = (int32_t)kept;
+    }
+    return 0;
+}
+
+// ---------------------------------------------------------------------------
+// Logical -> physical expert mapping with pruning  [UPD 功能说明, 参数说明]
+//
+// eplbTable [moeExpertNum, F] int32: column 0 = the number of instances
+// `count` of the row's logical expert, columns 1..count = their instance ids.
+//
+// Readings:
+//  * balancedExpertIds[b, k] = eplbTable[e, 1 + c] with e = expertIds[b, k]
+//    and c = localRankId % count (balanceMode 0, by rank) or b % count
+//    (balanceMode 1, by token); -1 when e is outside [0, moeExpertNum) or
+//    count is outside [1, F - 1].
+//  * With scales and thresholds: balancedActiveMask[b, k] = the token is
+//    active (activeMask[b], all active if not given) and
+//    f32(scale[b, k]) >= threshold[k] (pruned when below). Without them the
+//    mask is not written.
+//  * expertIds and the output are int32 (idBytes 4) or int64 (idBytes 8).
+// ---------------------------------------------------------------------------
+int oracle_update_expert(const void* expertIds, int32_t idBytes, const int32_t* table,
+                         const void* scales, int32_t scalesDtype, const float* threshold,
+                         const uint8_t* activeMask, int64_t BS, int64_t K, int64_t moeExpertNum,
+                         int64_t F, int64_t localRankId, int64_t balanceMode, void* balancedIds,
+                         uint8_t* balancedMask) {
+    if (BS <= 0 || K <= 0 || moeExpertNum <= 0 || F < 2) return 1;
+    for (int64_t b = 0; b < BS; ++b) {
+        for (int64_t k = 0; k < K; ++k) {
+            const int64_t i = b * K + k;
+            int64_t e;
+            if (idBytes == 8) {
+                int64_t v;
+                std::memcpy(&v, (const uint8_t*)expertIds + 8 * i, 8);
+                e = v;
+            } else {
+                int32_t v;
+                std::memcpy(&v, (const uint8_t*)expertIds + 4 * i, 4);
+                e = v;
+            }
+            int64_t out = -1;
+            if (e >= 0 && e < moeExpertNum) {
+                const int64_t count = table[e * F];
+                if (count >= 1 && count <= F - 1) {
+                    const int64_t c = (balanceMode == 0 ? localRankId : b) % count;
+                    out = table[e * F + 1 + c];
+                }
+            }
+            if (idBytes == 8) {
+                std::memcpy((uint8_t*)balancedIds + 8 * i, &out, 8);
+            } else {
+                const int32_t o = (int32_t)out;
+                std::memcpy((uint8_t*)balancedIds + 4 * i, &o, 4);
+            }
+            if (scales && threshold && balancedMask) {
+                const bool active = activeMask ? activeMask[b] != 0 : true;
+                const float sc = load_as_float(scales, i, scalesDtype);
+                balancedMask[i] = (active && !(sc < threshold[k])) ? 1 : 0;
+            }
+        }
     }
     return 0;
 }

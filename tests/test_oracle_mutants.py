@@ -100,6 +100,24 @@ MUTANTS = [
     ("double_weighting",
      "if (has_probs) term = x * p;\n                acc[(size_t)(t * H + h)] = acc[(size_t)(t * H + h)] + term;\n            }\n        }\n    } else {",
      "if (has_probs) term = (x * p) * p;\n                acc[(size_t)(t * H + h)] = acc[(size_t)(t * H + h)] + term;\n            }\n        }\n    } else {"),
+    ("update_modes_swapped",
+     "(balanceMode == 0 ? localRankId : b) % count",
+     "(balanceMode == 0 ? b : localRankId) % count"),
+    ("update_count_column_read",
+     "out = table[e * F + 1 + c];",
+     "out = table[e * F + c];"),
+    ("update_count_not_checked",
+     "if (count >= 1 && count <= F - 1) {",
+     "if (count >= 1) {"),
+    ("update_threshold_strict",
+     "(active && !(sc < threshold[k]))",
+     "(active && sc > threshold[k])"),
+    ("update_threshold_first_only",
+     "(active && !(sc < threshold[k]))",
+     "(active && !(sc < threshold[0]))"),
+    ("update_active_ignored",
+     "const bool active = activeMask ? activeMask[b] != 0 : true;",
+     "const bool active = true;"),
 ]
 
 
@@ -114,6 +132,7 @@ def test_pins_catch_mutant(name, old, new, tmp_path):
     r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
                         os.path.join(HERE, "test_oracle_pins.py"),
                         os.path.join(HERE, "test_oracle_context_pins.py"),
-                        os.path.join(HERE, "test_oracle_permute_pins.py")],
+                        os.path.join(HERE, "test_oracle_permute_pins.py"),
+                        os.path.join(HERE, "test_oracle_update_expert_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"

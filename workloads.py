@@ -294,3 +294,50 @@ def pack_schedule_context(*, sessions: int, micro: int, mbs: int, sel: int, expe
     ffn = np.array([info_ptr, info_size, data_ptr, data_size], dtype=np.uint64)
     ctx[CTX_FFN_OFFSET:CTX_FFN_OFFSET + 32] = ffn.view(np.uint8)
     return ctx
+
+
+# ---------------------------------------------------------------------------
+# MoeUpdateExpert inputs ("MoeUpdateExpert", 参数说明 and 约束说明)
+# ---------------------------------------------------------------------------
+
+def make_eplb_table(*, moe_expert_num: int, world_size: int, place_per_rank: int,
+                    seed: int = 0) -> np.ndarray:
+    """eplbTable [moeExpertNum, F] int32: column 0 the instance count (1 ..
+    worldSize), then the instance ids; every one of the worldSize *
+    place_per_rank instances hosts one logical expert (ids not repeated)."""
+    rng = _rng(seed, _TAG_ROUTE)
+    n_inst = world_size * place_per_rank
+    assert n_inst >= moe_expert_num
+    perm = rng.permutation(n_inst)
+    rows = [[int(perm[e])] for e in range(moe_expert_num)]
+    for inst in perm[moe_expert_num:]:
+        e = int(rng.integers(0, moe_expert_num))
+        if len(rows[e]) < world_size:
+            rows[e].append(int(inst))
+    F = max(len(r) for r in rows) + 1
+    table = np.zeros((moe_expert_num, F), dtype=np.int32)
+    for e, r in enumerate(rows):
+        table[e, 0] = len(r)
+        table[e, 1:1 + len(r)] = r
+    return table
+
+
+def make_update_expert(*, BS: int, K: int, moe_expert_num: int, world_size: int,
+                       place_per_rank: int, scales_dtype: int = DT_F32, id_dtype=np.int32,
+                       active_frac: float = 0.8, seed: int = 0) -> dict:
+    """Each token picks K distinct experts; scales descend within a token
+    (sorted softmax of N(0,1) logits); thresholds [K] float32; activeMask is a
+    prefix of trues."""
+    rng = _rng(seed, _TAG_IDS)
+    ids = np.stack([rng.choice(moe_expert_num, size=K, replace=False) for _ in range(BS)]).astype(id_dtype)
+    logits = _rng(seed, _TAG_PROBS).standard_normal((BS, K))
+    p = np.exp(logits - logits.max(axis=1, keepdims=True))
+    p = -np.sort(-(p / p.sum(axis=1, keepdims=True)), axis=1)
+    scales = _to_storage(p.astype(np.float32), scales_dtype)
+    threshold = np.full(K, 0.5 / K, dtype=np.float32)
+    active = np.zeros(BS, dtype=bool)
+    active[:int(round(active_frac * BS))] = True
+    table = make_eplb_table(moe_expert_num=moe_expert_num, world_size=world_size,
+                            place_per_rank=place_per_rank, seed=seed)
+    return dict(expert_ids=ids, table=table, scales=scales, scales_dtype=scales_dtype,
+                threshold=threshold, active=active, world_size=world_size)
