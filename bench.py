@@ -56,7 +56,7 @@ def parse_args(argv=None):
                     help="attention workers (A) of the oracle's bounded sample (full workload: 256)")
     ap.add_argument("--small", action="store_true", help="a small case of the same workload (profiling)")
     ap.add_argument("--workload", choices=["roundtrip", "tiny", "topk", "int8", "padded", "context",
-                                           "batching", "permute", "permute_padded"],
+                                           "batching", "permute", "permute_padded", "update_expert"],
                     default="roundtrip",
                     help="roundtrip (the bench line) or one of the other workloads, timed per call "
                          "with an L2 flush before each")
@@ -535,6 +535,23 @@ def run_workload(args):
             nonlocal out
             out = usc.moe_permute(xd, md, out=out, workspace=ws, **kw)
         phases = (0, 1)
+    elif name == "update_expert":
+        # MoeUpdateExpert at the page's maxima: remap + pruning of 512 x 16 ids
+        u = w.make_update_expert(**w.UPDATE_EXPERT)
+        BS, K = u["expert_ids"].shape
+        ids, tab, thr, act = g(u["expert_ids"]), g(u["table"]), g(u["threshold"]), g(u["active"])
+        sc = g(u["scales"].view(np.int16)).view(torch.bfloat16)
+        # ids, two table words, a bf16 scale, the threshold and the active flag
+        # read; an id and a mask byte written, per element
+        alg = BS * K * (4 + 8 + 2 + 4 + 1) + BS + K * 4
+        units, unit_name = BS, "tokens"
+        out = None
+
+        def call():
+            nonlocal out
+            out = usc.moe_update_expert(ids, tab, local_rank=3, world_size=u["world_size"], balance_mode=0,
+                                        scales=sc, threshold=thr, active=act, out=out)
+        phases = (0,)
     elif name in ("context", "batching"):
         # the round trip's batching alone, from flat arrays or from a
         # ScheduleContext (256 sessions x 4 micro-batches x 16 tokens x 9)

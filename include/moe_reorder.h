@@ -57,12 +57,17 @@ typedef int32_t mr_status;
 #define MR_DTYPE_BF16  1
 #define MR_DTYPE_INT8  2 /* int8 rows with an fp32 dynamic scale */
 #define MR_DTYPE_F32   3
+#define MR_DTYPE_INT32 4 /* expert ids of moe_update_expert */
+#define MR_DTYPE_INT64 5
 
 /* Sentinel-free limits from the pages' constraint tables. */
 #define MR_MAX_EXPERT_NUM 8192 /* expertNum in (0, 8192] */
 #define MR_MAX_A          1024 /* A in (0, 1024] */
 #define MR_MAX_TOPK1      64   /* topK+1 in (0, 64] */
 #define MR_MAX_TOPK_NUM   512  /* unpermute topK_num <= 512 */
+#define MR_MAX_UPDATE_BS      512  /* moe_update_expert: BS in (0, 512] */
+#define MR_MAX_UPDATE_K       16   /* K in (0, 16], K <= moeExpertNum */
+#define MR_MAX_UPDATE_EXPERTS 1024 /* moeExpertNum in (0, 1024] */
 
 /* ------------------------------------------------------------------------ */
 /* FFN-worker batching                                                      */
@@ -343,6 +348,56 @@ mr_status moe_permute(const void* tokens, const int8_t* routingMap, int64_t numT
                       int32_t paddedMode, int64_t capacity, void* permutedTokens,
                       int32_t* sortedIndices, int32_t* permutedRowsOut, void* workspace,
                       uint64_t workspaceSize, void* stream);
+
+/*
+ * moe_update_expert
+ *   "MoeUpdateExpert", 功能说明 and 参数说明: maps each token's top-K logical
+ *   expert ids to physical expert instances through the EPLB table (load
+ *   balancing), and prunes a token's experts whose scale is below a threshold.
+ *   The page gives no formula for the choice of instance; this library reads
+ *   "by rank" and "by token" as
+ *     balancedExpertIds[b,k] = eplbTable[e, 1 + c], e = expertIds[b,k],
+ *     count = eplbTable[e, 0], c = localRankId mod count (balanceMode 0) or
+ *     c = b mod count (balanceMode 1);
+ *   -1 when e is outside [0, moeExpertNum) or count outside [1, F - 1] (no
+ *   read leaves the table). With scales and threshold:
+ *     balancedActiveMask[b,k] = activeMask[b] && !(f32(scale[b,k]) < threshold[k])
+ *   (equal is kept; activeMask NULL means every token is active).
+ *
+ *   Inputs (device pointers):
+ *   expertIds          [BS, K] of idDtype (MR_DTYPE_INT32 or MR_DTYPE_INT64).
+ *   eplbTable          int32 [moeExpertNum, F]: column 0 the instance count,
+ *                      columns 1..count the instance ids.
+ *   expertScales       [BS, K] of scalesDtype (F16, BF16, F32), nullable;
+ *                      NULL iff pruningThreshold is NULL.
+ *   pruningThreshold   float32 [K], nullable.
+ *   activeMask         bool (one byte, nonzero = true) [BS], nullable; needs
+ *                      expertScales. The page asks that the trues come first;
+ *                      the result does not depend on it.
+ *   BS in (0, 512]; K in (0, 16], K <= moeExpertNum; moeExpertNum in
+ *   (0, 1024]; balanceMode 0: worldSize in [2, 768], localRankId in
+ *   [0, worldSize); balanceMode 1: worldSize in [1, 1024], localRankId unused;
+ *   F in [2, worldSize + 1].
+ *   strides            host array of 12 int64 element strides, nullable (NULL:
+ *                      contiguous): expertIds (b, k), eplbTable (e, f),
+ *                      expertScales (b, k), pruningThreshold (k), activeMask
+ *                      (b), balancedExpertIds (b, k), balancedActiveMask (b, k).
+ *                      Input strides >= 0 (0 broadcasts), output strides >= 1.
+ *                      Read during the call only.
+ *   Outputs (device pointers):
+ *   balancedExpertIds  [BS, K] of idDtype.
+ *   balancedActiveMask bool [BS, K]; required with expertScales, not written
+ *                      without.
+ *   stream             cudaStream_t (NULL: the legacy default stream). No
+ *                      workspace is needed.
+ *   Returns MR_OK, MR_ERR_PARAM_NULLPTR, MR_ERR_PARAM_INVALID or MR_ERR_CUDA.
+ */
+mr_status moe_update_expert(const void* expertIds, int32_t idDtype, const int32_t* eplbTable,
+                            const void* expertScales, int32_t scalesDtype,
+                            const float* pruningThreshold, const uint8_t* activeMask, int64_t BS,
+                            int64_t K, int64_t moeExpertNum, int64_t F, int64_t localRankId,
+                            int64_t worldSize, int64_t balanceMode, const int64_t* strides,
+                            void* balancedExpertIds, uint8_t* balancedActiveMask, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Utilities (no counterpart on the pages)                                  */

@@ -277,3 +277,42 @@ def test_permute_workspace_size(L):
     assert ws.value > 0
     assert L.moe_permute_get_workspace_size(16384, 4096, 0, 128, 0, 1, 512, ctypes.byref(ws)) == OK
     assert L.moe_permute_get_workspace_size(16, 32, 1, 8, 2, 0, 0, None) == NULLPTR
+
+
+def _update_call(L, **kw):
+    a = dict(ids=FAKE, idt=4, tab=FAKE, sc=None, sdt=3, thr=None, act=None, BS=8, K=4, E=16, F=3,
+             rank=1, ws=4, mode=0, strides=None, out=FAKE, mask=None, stream=None)
+    a.update(kw)
+    return L.moe_update_expert(a["ids"], a["idt"], a["tab"], a["sc"], a["sdt"], a["thr"], a["act"],
+                               a["BS"], a["K"], a["E"], a["F"], a["rank"], a["ws"], a["mode"],
+                               a["strides"], a["out"], a["mask"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,expect", [
+    (dict(ids=None), NULLPTR),
+    (dict(tab=None), NULLPTR),
+    (dict(out=None), NULLPTR),
+    (dict(sc=FAKE), NULLPTR),                         # scales without threshold
+    (dict(thr=FAKE), NULLPTR),                        # threshold without scales
+    (dict(act=FAKE), NULLPTR),                        # activeMask without scales
+    (dict(sc=FAKE, thr=FAKE), NULLPTR),               # pruning without a mask output
+    (dict(sc=FAKE, thr=FAKE, mask=FAKE, sdt=2), INVALID),
+    (dict(idt=3), INVALID),
+    (dict(BS=0), INVALID),
+    (dict(BS=513), INVALID),
+    (dict(K=17, E=32), INVALID),
+    (dict(K=5, E=4), INVALID),                        # K > moeExpertNum
+    (dict(E=1025), INVALID),
+    (dict(mode=2), INVALID),
+    (dict(ws=1), INVALID),                            # by rank: worldSize >= 2
+    (dict(ws=769, F=3), INVALID),
+    (dict(rank=4), INVALID),                          # localRankId >= worldSize
+    (dict(rank=-1), INVALID),
+    (dict(F=1), INVALID),
+    (dict(F=6), INVALID),                             # F > worldSize + 1
+    (dict(mode=1, ws=0), INVALID),
+    (dict(strides=_native.int64_array([4, 1, 3, 1, 4, 1, 1, 1, 4, 0, 4, 1])), INVALID),  # output stride 0
+    (dict(strides=_native.int64_array([4, -1, 3, 1, 4, 1, 1, 1, 4, 1, 4, 1])), INVALID),
+])
+def test_update_expert_validation(L, kw, expect):
+    assert _update_call(L, **kw) == expect

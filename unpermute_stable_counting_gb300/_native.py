@@ -34,6 +34,8 @@ SIGNATURES = {
     "moe_permute_get_workspace_size": (_I32, [_I64, _I64, _I32, _I64, _I64, _I32, _I64, _PU64]),
     "moe_permute": (_I32, [_P, _P, _I64, _I64, _I32, _I64, _I64, _I32, _I64, _P, _P, _P, _P, _U64,
                            _P]),
+    "moe_update_expert": (_I32, [_P, _I32, _P, _P, _I32, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64,
+                                 _I64, _PI64, _P, _P, _P]),
     "mr_status_string": (ctypes.c_char_p, [_I32]),
     "mr_version": (_I32, []),
     "mr_profile_set_events": (_I32, [ctypes.POINTER(_P), _I32]),

@@ -38,12 +38,12 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _require_cuda(name, t, dtype=None):
+def _require_cuda(name, t, dtype=None, strided=False):
     if t is None:
         return
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
-    if not t.is_contiguous():
+    if not strided and not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
         raise TypeError(f"{name} must have dtype {dtype}, got {t.dtype}")
@@ -101,7 +101,7 @@ def ffnwb_batching(expert_ids, token_data, session_ids, micro_batch_ids, *, expe
                     ("micro_batch_ids", micro_batch_ids), ("token_ids", token_ids)):
         _require_cuda(name, t, torch.int32)
     _require_cuda("token_data", token_data)
-    _require_cuda("scales", scales)
+    _require_cuda("scales", scales, strided=True)
     if token_row_stride is None:
         token_row_stride = token_data.stride(0) * token_data.element_size()
     dev = token_data.device
@@ -269,6 +269,50 @@ def moe_permute(tokens, routing_map, *, topk: int = 0, padded_mode: bool = False
                            _ptr(out["sortedIndices"]), _ptr(out.get("permutedRows")),
                            _ptr(workspace), int(workspace.numel()), _stream(stream, dev))
     _check(st, "moe_permute")
+    return out
+
+
+_ID_TO_DT = {torch.int32: 4, torch.int64: 5}
+
+
+def moe_update_expert(expert_ids, eplb_table, *, local_rank: int = 0, world_size: int,
+                      balance_mode: int = 0, scales=None, threshold=None, active=None,
+                      out: dict | None = None, stream=None) -> dict:
+    """Map expert_ids [BS, K] (int32/int64) to physical instances through
+    eplb_table [E, F] int32 and, with scales [BS, K] and threshold [K] (or
+    [1, K]), prune them. Strided views are passed by their strides (no copy).
+    Returns balancedExpertIds and balancedActiveMask (None without scales)."""
+    _require_cuda("expert_ids", expert_ids, (torch.int32, torch.int64), strided=True)
+    _require_cuda("eplb_table", eplb_table, (torch.int32,), strided=True)
+    BS, K = int(expert_ids.shape[0]), int(expert_ids.shape[1])
+    E, F = int(eplb_table.shape[0]), int(eplb_table.shape[1])
+    dev = expert_ids.device
+    sdt = 3
+    if scales is not None:
+        _require_cuda("scales", scales, strided=True)
+        sdt = _TORCH_TO_DT.get(scales.dtype)
+        if sdt is None:
+            raise TypeError(f"scales dtype {scales.dtype} is not f16/bf16/f32")
+    if threshold is not None:
+        _require_cuda("threshold", threshold, (torch.float32,), strided=True)
+    if active is not None:
+        _require_cuda("active", active, (torch.bool, torch.uint8), strided=True)
+    if out is None:
+        out = dict(balancedExpertIds=torch.empty((BS, K), dtype=expert_ids.dtype, device=dev),
+                   balancedActiveMask=(torch.empty((BS, K), dtype=torch.bool, device=dev)
+                                       if scales is not None else None))
+    bal, msk = out["balancedExpertIds"], out.get("balancedActiveMask")
+    z = (0, 0)
+    strides = (tuple(expert_ids.stride()) + tuple(eplb_table.stride())
+               + (tuple(scales.stride()) if scales is not None else z)
+               + ((threshold.stride(-1),) if threshold is not None else (0,))
+               + ((active.stride(0),) if active is not None else (0,))
+               + tuple(bal.stride()) + (tuple(msk.stride()) if msk is not None else (1, 1)))
+    st = lib().moe_update_expert(_ptr(expert_ids), _ID_TO_DT[expert_ids.dtype], _ptr(eplb_table),
+                                 _ptr(scales), sdt, _ptr(threshold), _ptr(active), BS, K, E, F,
+                                 int(local_rank), int(world_size), int(balance_mode),
+                                 int64_array(strides), _ptr(bal), _ptr(msk), _stream(stream, dev))
+    _check(st, "moe_update_expert")
     return out
 
 

@@ -341,3 +341,9 @@ def make_update_expert(*, BS: int, K: int, moe_expert_num: int, world_size: int,
                             place_per_rank=place_per_rank, seed=seed)
     return dict(expert_ids=ids, table=table, scales=scales, scales_dtype=scales_dtype,
                 threshold=threshold, active=active, world_size=world_size)
+
+
+# The page's maxima (BS 512, K 16) with 512 logical experts over 128 ranks x 8
+# instances: 1024 instances, so experts are replicated up to the rank count.
+UPDATE_EXPERT = dict(BS=512, K=16, moe_expert_num=512, world_size=128, place_per_rank=8,
+                     scales_dtype=DT_BF16, seed=6)
