@@ -68,11 +68,11 @@ def _load():
         lib.oracle_batching.argtypes = [
             _P, _I32, _P, _I64, _P, _I64, _P, _P, _P,
             _I64, _I64, _I64, _I64, _I64, _I64, _I64,
-            _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+            _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32]
         lib.oracle_batching_context.restype = _I32
         lib.oracle_batching_context.argtypes = [
             _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _I64, _I64, _I64,
-            _P, _P, _P, _P, _P, _P, _P, _P, _P]
+            _P, _P, _P, _P, _P, _P, _P, _P, _P, _I32]
         lib.oracle_permute.restype = _I32
         lib.oracle_permute.argtypes = [_P, _P, _I64, _I64, _I32, _I64, _I64, _I32, _I64, _P, _P, _P]
         lib.oracle_update_expert.restype = _I32
@@ -132,11 +132,12 @@ def float_to_bf16(x: np.ndarray) -> np.ndarray:
 ELEM_BYTES = {0: 2, 1: 2, 2: 1, 3: 4}
 
 
-def batching(inp: dict, *, with_gather_idx: bool = False) -> dict:
+def batching(inp: dict, *, with_gather_idx: bool = False, full_tail: bool = False) -> dict:
     """Run the batching oracle on a ``workloads.make_batching`` dict.
     Returns y (uint8 [Y, H*s]), groupList, sessionIds, microBatchIds, tokenIds,
     expertOffsets, dynamicScale (None unless int8), actualTokenNum (int),
-    sortedIndices (slot -> output row or -1) and optionally gather_idx."""
+    sortedIndices (slot -> output row or -1) and optionally gather_idx.
+    full_tail applies the gather and the id lookups to the masked rows too."""
     Y, H, dt = inp["Y"], inp["H"], inp["tokenDtype"]
     E = inp["expertNum"]
     row_bytes = H * ELEM_BYTES[dt]
@@ -159,7 +160,7 @@ def batching(inp: dict, *, with_gather_idx: bool = False) -> dict:
         _ptr(inp["session_in"]), _ptr(inp["micro_in"]), _ptr(inp.get("token_in")),
         E, inp["A"], inp["BS"], inp["K1"], H, dt, inp["layerNum"],
         _ptr(y), _ptr(gl), _ptr(sess), _ptr(micro), _ptr(tok), _ptr(eoff), _ptr(dyn),
-        _ptr(atn), _ptr(sidx), _ptr(gidx))
+        _ptr(atn), _ptr(sidx), _ptr(gidx), int(bool(full_tail)))
     if rc != 0:
         raise ValueError(f"oracle_batching rejected its arguments (code {rc})")
     out = dict(y=y, groupList=gl, sessionIds=sess, microBatchIds=micro, tokenIds=tok,
@@ -172,9 +173,10 @@ def batching(inp: dict, *, with_gather_idx: bool = False) -> dict:
 
 def batching_context(ctx: np.ndarray, token_info: np.ndarray, token_data: np.ndarray, *,
                      expertNum: int, maxOutShape, tokenDtype: int, needSchedule: int,
-                     layerNum: int) -> dict:
+                     layerNum: int, full_tail: bool = False) -> dict:
     """Run the ScheduleContext batching oracle. ctx: the 1024 context bytes;
-    token_info / token_data: host copies of the buffers the context points to."""
+    token_info / token_data: host copies of the buffers the context points to.
+    full_tail: as for ``batching``, for the slots the context holds."""
     A, BS, K1, H = (int(v) for v in maxOutShape)
     Y, E = A * BS * K1, int(expertNum)
     row_bytes = H * ELEM_BYTES[tokenDtype]
@@ -188,7 +190,7 @@ def batching_context(ctx: np.ndarray, token_info: np.ndarray, token_data: np.nda
         _ptr(np.ascontiguousarray(ctx, dtype=np.uint8)), _ptr(np.ascontiguousarray(token_info)),
         _ptr(np.ascontiguousarray(token_data)), E, A, BS, K1, H, int(tokenDtype), int(needSchedule),
         int(layerNum), _ptr(y), _ptr(gl), _ptr(sess), _ptr(micro), _ptr(tok), _ptr(eoff), _ptr(dyn),
-        _ptr(atn), _ptr(status))
+        _ptr(atn), _ptr(status), int(bool(full_tail)))
     if rc != 0:
         raise ValueError(f"oracle_batching_context rejected its arguments (code {rc})")
     return dict(y=y, groupList=gl, sessionIds=sess, microBatchIds=micro, tokenIds=tok,

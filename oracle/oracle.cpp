@@ -18,8 +18,8 @@
 //   [UPD]  "MoeUpdateExpert" (CANN ops-transformer README): 功能说明,
 //          参数说明 and 约束说明.
 //
-// Readings where the pages are silent or garbled are listed in the design doc and
-// restated at each use below.
+// Where the pages are silent or garbled, the reading taken is stated at each
+// use below.
 //
 // Floating point: the pages fix the arithmetic of the reduction (operands cast
 // to fp32, multiply by the prob, add, one final cast with round-to-nearest-
@@ -182,7 +182,7 @@ void oracle_float_to_bf16(const float* in, uint16_t* out, int64_t n) {
 //   group_list[e] = [expert_id_e, expert_token_num_e]
 //   actual_token_num = sum_e expert_token_num_e
 //
-// Readings (see DESIGN.md):
+// Readings:
 //  * Y = A * BS * (topK+1)   (maxOutShape row of 参数说明).
 //  * key(s) = layer_id * E_l + expert_ids[s] when 0 <= expert_ids[s] < E_l,
 //    else the sentinel E (masked). E_l = expertNum / max(layerNum, 1).
@@ -209,7 +209,7 @@ int oracle_batching(const int32_t* expert_ids, int32_t layer_id, const uint8_t* 
                     int64_t tokenDtype, int64_t layerNum, uint8_t* y, int64_t* group_list,
                     int32_t* session_out, int32_t* micro_out, int32_t* token_out,
                     int32_t* expert_offsets, float* dynamic_scale, int64_t* actual_token_num,
-                    int32_t* sorted_indices_out, int32_t* gather_idx_out) {
+                    int32_t* sorted_indices_out, int32_t* gather_idx_out, int32_t full_tail) {
     if (expertNum <= 0 || A <= 0 || BS <= 0 || K1 <= 0 || H <= 0) return 1;
     if (tokenDtype != DT_F16 && tokenDtype != DT_BF16 && tokenDtype != DT_INT8) return 2;
     const int64_t Y = A * BS * K1;
@@ -236,8 +236,10 @@ int oracle_batching(const int32_t* expert_ids, int32_t layer_id, const uint8_t* 
     int64_t U = 0;
     for (int64_t s = 0; s < Y; ++s) U += key[s] < E ? 1 : 0;
 
-    // y[i] = token_data[gather_idx[i]] for the unmasked prefix
-    for (int64_t i = 0; i < U; ++i) {
+    // y[i] = token_data[gather_idx[i]] for the unmasked prefix (every row
+    // when the formula is applied to the masked tail too)
+    const int64_t gathered = full_tail ? Y : U;
+    for (int64_t i = 0; i < gathered; ++i) {
         const int64_t g = gather_idx[i];
         std::memcpy(y + (size_t)(i * row_bytes), token_data + (size_t)(g * row_stride),
                     (size_t)row_bytes);
@@ -258,6 +260,12 @@ int oracle_batching(const int32_t* expert_ids, int32_t layer_id, const uint8_t* 
             micro_out[i] = micro_in[g];
             token_out[i] = token_in ? token_in[g] : (int32_t)g;
             expert_offsets[i] = (int32_t)(i - group_start);
+        } else if (full_tail) {
+            // a masked slot's own ids; it belongs to no expert group
+            session_out[i] = session_in[g];
+            micro_out[i] = micro_in[g];
+            token_out[i] = token_in ? token_in[g] : (int32_t)g;
+            expert_offsets[i] = -1;
         } else {
             session_out[i] = -1;
             micro_out[i] = -1;
@@ -311,7 +319,7 @@ int oracle_batching(const int32_t* expert_ids, int32_t layer_id, const uint8_t* 
 // selected_expert_num i32 expert ids. token_data_buf holds one row per slot in
 // the same order.
 //
-// Readings (see DESIGN.md):
+// Readings:
 //  * The slots are the blocks' expert ids in block order; slot g of block b
 //    has session id b / micro_batch_num, micro-batch id b % micro_batch_num
 //    and token id g.
@@ -326,6 +334,9 @@ int oracle_batching(const int32_t* expert_ids, int32_t layer_id, const uint8_t* 
 //    are int32): then every slot is masked and status = -1.
 //  * Outputs are sized for Y rows; rows past the context's slots belong to
 //    the masked tail (ids -1, y untouched).
+//  * full_tail: the formulas of 计算公式 are applied to the masked rows too,
+//    as far as they have a slot in token_data_buf: y, the scale, session,
+//    micro-batch and token ids of the slot; expertOffsets stays -1.
 // The host copies of token_info_buf / token_data_buf are passed separately
 // (the context itself holds device addresses).
 // ---------------------------------------------------------------------------
@@ -335,7 +346,7 @@ int oracle_batching_context(const uint8_t* ctx, const uint8_t* token_info,
                             int64_t layerNum, uint8_t* y, int64_t* group_list,
                             int32_t* session_out, int32_t* micro_out, int32_t* token_out,
                             int32_t* expert_offsets, float* dynamic_scale,
-                            int64_t* actual_token_num, int32_t* status) {
+                            int64_t* actual_token_num, int32_t* status, int32_t full_tail) {
     if (expertNum <= 0 || A <= 0 || BS <= 0 || K1 <= 0 || H <= 0) return 1;
     const int64_t Y = A * BS * K1;
     const int64_t E = expertNum;
@@ -389,8 +400,11 @@ int oracle_batching_context(const uint8_t* ctx, const uint8_t* token_info,
                      [&](int64_t a, int64_t b) { return key[a] < key[b]; });
     int64_t U = 0;
     for (int64_t s = 0; s < Y; ++s) U += key[s] < E ? 1 : 0;
-    for (int64_t i = 0; i < U; ++i) {
+    // slots with a row in token_data_buf (none when the context is invalid)
+    const int64_t n_src = valid ? slots : 0;
+    for (int64_t i = 0; i < Y; ++i) {
         const int64_t g = gather_idx[i];
+        if (!(i < U || (full_tail && g < n_src))) continue;
         std::memcpy(y + i * row_bytes, token_data + g * row_stride, (size_t)row_bytes);
         if (tokenDtype == DT_INT8) std::memcpy(&dynamic_scale[i], token_data + g * row_stride + row_bytes, 4);
     }
@@ -403,6 +417,11 @@ int oracle_batching_context(const uint8_t* ctx, const uint8_t* token_info,
             micro_out[i] = mb[g];
             token_out[i] = (int32_t)g;
             expert_offsets[i] = (int32_t)(i - group_start);
+        } else if (full_tail && g < n_src) {
+            session_out[i] = sess[g];
+            micro_out[i] = mb[g];
+            token_out[i] = (int32_t)g;
+            expert_offsets[i] = -1;
         } else {
             session_out[i] = micro_out[i] = token_out[i] = expert_offsets[i] = -1;
         }
@@ -427,7 +446,7 @@ int oracle_batching_context(const uint8_t* ctx, const uint8_t* token_info,
 // unpermute rearranges the tokens by routingMap into an expert-grouped compact
 // layout, permutedTokens, so that each expert reads its tokens contiguously]
 //
-// Readings (see DESIGN.md), chosen so that the unpermute takes these outputs:
+// Readings, chosen so that the unpermute takes these outputs:
 //  * Not padded: the rows are the (token, expert) pairs with routingMap = 1 in
 //    expert-major order (expert ascending, then token ascending): the order of
 //    probs.T.maskedSelect(routingMap.T). permutedTokens[r] = tokens[t(r)] for
@@ -501,7 +520,7 @@ int oracle_permute(const void* tokens, const int8_t* routingMap, int64_t T, int6
 // eplbTable [moeExpertNum, F] int32: column 0 = the number of instances
 // `count` of the row's logical expert, columns 1..count = their instance ids.
 //
-// Readings (see DESIGN.md):
+// Readings:
 //  * balancedExpertIds[b, k] = eplbTable[e, 1 + c] with e = expertIds[b, k]
 //    and c = localRankId % count (balanceMode 0, by rank) or b % count
 //    (balanceMode 1, by token); -1 when e is outside [0, moeExpertNum) or
@@ -569,7 +588,7 @@ int oracle_update_expert(const void* expertIds, int32_t idBytes, const int32_t* 
 // (3) no probs, padded:   as (1) without the weight
 // (4) no probs, !padded:  as (2) without the weight
 //
-// Readings (see DESIGN.md):
+// Readings:
 //  * "+=" accumulates (the page's text says 累加求和 throughout).
 //  * One multiplication per term, by the slot's (2) or the row's (1) prob.
 //  * A term is skipped unless its index is valid (IsValidInputIndex) and, with

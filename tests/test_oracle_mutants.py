@@ -118,6 +118,24 @@ MUTANTS = [
     ("update_active_ignored",
      "const bool active = activeMask ? activeMask[b] != 0 : true;",
      "const bool active = true;"),
+    ("full_tail_rows_ignored",
+     "const int64_t gathered = full_tail ? Y : U;",
+     "const int64_t gathered = U;"),
+    ("full_tail_last_row_dropped",
+     "const int64_t gathered = full_tail ? Y : U;",
+     "const int64_t gathered = full_tail ? Y - 1 : U;"),
+    ("full_tail_ids_not_looked_up",
+     "} else if (full_tail) {",
+     "} else if (false) {"),
+    ("full_tail_offsets_not_minus_one",
+     "token_out[i] = token_in ? token_in[g] : (int32_t)g;\n            expert_offsets[i] = -1;",
+     "token_out[i] = token_in ? token_in[g] : (int32_t)g;\n            expert_offsets[i] = 0;"),
+    ("context_full_tail_rows_ignored",
+     "if (!(i < U || (full_tail && g < n_src))) continue;",
+     "if (!(i < U)) continue;"),
+    ("context_full_tail_ids_not_looked_up",
+     "} else if (full_tail && g < n_src) {",
+     "} else if (false) {"),
 ]
 
 
@@ -133,6 +151,7 @@ def test_pins_catch_mutant(name, old, new, tmp_path):
                         os.path.join(HERE, "test_oracle_pins.py"),
                         os.path.join(HERE, "test_oracle_context_pins.py"),
                         os.path.join(HERE, "test_oracle_permute_pins.py"),
-                        os.path.join(HERE, "test_oracle_update_expert_pins.py")],
+                        os.path.join(HERE, "test_oracle_update_expert_pins.py"),
+                        os.path.join(HERE, "test_oracle_full_tail_pins.py")],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
