@@ -155,6 +155,30 @@ mr_status ffnwb_batching(const int32_t* expertIds, int32_t layerId, const void* 
                          uint64_t workspaceSize, void* stream);
 
 /*
+ * ffnwb_batching_ex
+ *   ffnwb_batching with option flags (before the workspace arguments).
+ *   MR_BATCHING_FULL_TAIL: apply 计算公式's y[i] = token_data[gather_idx[i]]
+ *   and step 3's id lookup to the masked rows too: rows i >= U get the row,
+ *   the INT8 scale and the session / micro-batch / token ids of the masked
+ *   slot they hold (masked slots in ascending slot order); expertOffsets stays
+ *   -1 there (a masked row is in no expert group). groupList, actualTokenNum
+ *   and sortedIndicesOut are those of ffnwb_batching. Costs (Y - U) more row
+ *   copies. Other flag bits: MR_ERR_PARAM_INVALID. ffnwb_batching is this call
+ *   with flags 0; the workspace size is the same.
+ */
+#define MR_BATCHING_FULL_TAIL 1u
+mr_status ffnwb_batching_ex(const int32_t* expertIds, int32_t layerId, const void* tokenData,
+                            int64_t tokenRowStride, const void* scales, int64_t scaleStride,
+                            const int32_t* sessionIdsIn, const int32_t* microBatchIdsIn,
+                            const int32_t* tokenIdsIn, int64_t expertNum,
+                            const int64_t* maxOutShape, int64_t tokenDtype, int64_t needSchedule,
+                            int64_t layerNum, void* y, int64_t* groupList, int32_t* sessionIds,
+                            int32_t* microBatchIds, int32_t* tokenIds, int32_t* expertOffsets,
+                            float* dynamicScale, int64_t* actualTokenNum,
+                            int32_t* sortedIndicesOut, uint32_t flags, void* workspace,
+                            uint64_t workspaceSize, void* stream);
+
+/*
  * ffnwb_batching_context_get_workspace_size / ffnwb_batching_context
  *   "aclnnFfnWorkerBatching", 功能说明 step 1 (read the FFN side's data area),
  *   参数说明 (scheduleContext, needSchedule) and the ScheduleContext /
@@ -200,6 +224,23 @@ mr_status ffnwb_batching_context(const void* scheduleContext, int64_t expertNum,
                                  float* dynamicScale, int64_t* actualTokenNum,
                                  int32_t* scheduleStatus, void* workspace, uint64_t workspaceSize,
                                  void* stream);
+/*
+ * ffnwb_batching_context_ex
+ *   ffnwb_batching_context with option flags (before the workspace
+ *   arguments); MR_BATCHING_FULL_TAIL as for ffnwb_batching_ex, for the slots
+ *   the context holds: rows for slots past the context's (or every row of a
+ *   context that does not fit) stay untouched, ids -1. ffnwb_batching_context
+ *   is this call with flags 0.
+ */
+mr_status ffnwb_batching_context_ex(const void* scheduleContext, int64_t expertNum,
+                                    const int64_t* maxOutShape, int64_t tokenDtype,
+                                    int64_t needSchedule, int64_t layerNum, int64_t waitTimeoutUs,
+                                    void* y, int64_t* groupList, int32_t* sessionIds,
+                                    int32_t* microBatchIds, int32_t* tokenIds,
+                                    int32_t* expertOffsets, float* dynamicScale,
+                                    int64_t* actualTokenNum, int32_t* scheduleStatus,
+                                    uint32_t flags, void* workspace, uint64_t workspaceSize,
+                                    void* stream);
 
 /*
  * ffnwb_batching_noalloc -- the batching for callers that cannot allocate.

@@ -316,3 +316,41 @@ def _update_call(L, **kw):
 ])
 def test_update_expert_validation(L, kw, expect):
     assert _update_call(L, **kw) == expect
+
+
+@pytest.mark.parametrize("flags,kw,expect", [
+    (2, {}, INVALID),                                 # unknown option bit
+    (0x80000000, {}, INVALID),
+    (1, dict(wsz=16), WORKSPACE),                     # the option keeps the workspace size
+    (1, dict(ns=1), UNSUPPORTED),
+    (1, dict(y=None), NULLPTR),
+])
+def test_batching_ex_flags(L, flags, kw, expect):
+    a = dict(expertIds=FAKE, layerId=0, tokenData=FAKE, stride=256, scales=None, scaleStride=4,
+             sess=FAKE, micro=FAKE, tok=None, E=8, shape=(2, 8, 3, 128), dt=0, ns=0, ln=1, y=FAKE,
+             gl=FAKE, so=FAKE, mo=FAKE, to=FAKE, eo=FAKE, dyn=None, atn=FAKE, sidx=None,
+             ws=FAKE, wsz=1 << 40, stream=None)
+    a.update(kw)
+    st = L.ffnwb_batching_ex(a["expertIds"], a["layerId"], a["tokenData"], a["stride"], a["scales"],
+                             a["scaleStride"], a["sess"], a["micro"], a["tok"], a["E"],
+                             _native.int64_array(a["shape"]), a["dt"], a["ns"], a["ln"], a["y"],
+                             a["gl"], a["so"], a["mo"], a["to"], a["eo"], a["dyn"], a["atn"],
+                             a["sidx"], flags, a["ws"], a["wsz"], a["stream"])
+    assert st == expect
+
+
+@pytest.mark.parametrize("flags,kw,expect", [
+    (4, {}, INVALID),
+    (1, dict(wsz=8), WORKSPACE),
+    (1, dict(ctx=None), NULLPTR),
+])
+def test_context_ex_flags(L, flags, kw, expect):
+    a = dict(ctx=ctypes.c_void_p(0x1000), E=8, shape=(2, 8, 3, 128), dt=0, ns=0, ln=1, timeout=1000,
+             y=FAKE, gl=FAKE, so=FAKE, mo=FAKE, to=FAKE, eo=FAKE, dyn=None, atn=FAKE, status=None,
+             ws=FAKE, wsz=1 << 40, stream=None)
+    a.update(kw)
+    st = L.ffnwb_batching_context_ex(a["ctx"], a["E"], _native.int64_array(a["shape"]), a["dt"],
+                                     a["ns"], a["ln"], a["timeout"], a["y"], a["gl"], a["so"], a["mo"],
+                                     a["to"], a["eo"], a["dyn"], a["atn"], a["status"], flags, a["ws"],
+                                     a["wsz"], a["stream"])
+    assert st == expect

@@ -14,6 +14,7 @@ _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
 _I32 = ctypes.c_int32
 _U64 = ctypes.c_uint64
+_U32 = ctypes.c_uint32
 _PI64 = ctypes.POINTER(ctypes.c_int64)
 _PU64 = ctypes.POINTER(ctypes.c_uint64)
 
@@ -22,9 +23,13 @@ SIGNATURES = {
     "ffnwb_batching_get_workspace_size": (_I32, [_I64, _PI64, _I64, _I64, _I64, _PU64]),
     "ffnwb_batching": (_I32, [_P, _I32, _P, _I64, _P, _I64, _P, _P, _P, _I64, _PI64, _I64, _I64,
                               _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _U64, _P]),
+    "ffnwb_batching_ex": (_I32, [_P, _I32, _P, _I64, _P, _I64, _P, _P, _P, _I64, _PI64, _I64, _I64,
+                                 _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _U32, _P, _U64, _P]),
     "ffnwb_batching_context_get_workspace_size": (_I32, [_I64, _PI64, _I64, _I64, _I64, _PU64]),
     "ffnwb_batching_context": (_I32, [_P, _I64, _PI64, _I64, _I64, _I64, _I64, _P, _P, _P, _P, _P,
                                       _P, _P, _P, _P, _P, _U64, _P]),
+    "ffnwb_batching_context_ex": (_I32, [_P, _I64, _PI64, _I64, _I64, _I64, _I64, _P, _P, _P, _P,
+                                         _P, _P, _P, _P, _P, _U32, _P, _U64, _P]),
     "ffnwb_batching_noalloc": (_I32, [_P, _I32, _P, _I64, _P, _I64, _P, _P, _P, _I64, _PI64, _I64,
                                       _I64, _I64, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
     "moe_unpermute_get_workspace_size": (_I32, [_I64, _I64, _I32, _I64, _I32, _I32, _I64, _I64,

@@ -20,6 +20,7 @@ _DT_TO_TORCH = {DT_F16: torch.float16, DT_BF16: torch.bfloat16, DT_INT8: torch.i
 _ELEM = {DT_F16: 2, DT_BF16: 2, DT_INT8: 1, DT_F32: 4}
 
 MR_OK = 0
+MR_BATCHING_FULL_TAIL = 1
 
 
 class MoeReorderError(RuntimeError):
@@ -89,11 +90,12 @@ def ffnwb_batching(expert_ids, token_data, session_ids, micro_batch_ids, *, expe
                    max_out_shape, token_dtype: int, layer_num: int = 1, layer_id: int = 0,
                    token_ids=None, scales=None, scale_stride: int = 4, token_row_stride=None,
                    need_schedule: int = 0, with_sorted_indices: bool = False, out: dict | None = None,
-                   workspace=None, stream=None) -> dict:
+                   workspace=None, stream=None, full_tail: bool = False) -> dict:
     """Run the batching on the current CUDA stream.
 
     token_data: CUDA tensor whose first dimension is the Y slots; row s starts
     at token_row_stride bytes * s (default: the tensor's own row stride).
+    full_tail: also gather the rows (and ids) of the masked slots.
     Returns the output dict (see batching_outputs)."""
     A, BS, K1, H = (int(v) for v in max_out_shape)
     Y = A * BS * K1
@@ -111,14 +113,17 @@ def ffnwb_batching(expert_ids, token_data, session_ids, micro_batch_ids, *, expe
         ws = batching_workspace_size(expert_num, max_out_shape, token_dtype, layer_num, need_schedule)
         workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
     shape = int64_array(max_out_shape)
-    st = lib().ffnwb_batching(
-        _ptr(expert_ids), int(layer_id), _ptr(token_data), int(token_row_stride), _ptr(scales),
-        int(scale_stride), _ptr(session_ids), _ptr(micro_batch_ids), _ptr(token_ids),
-        int(expert_num), shape, int(token_dtype), int(need_schedule), int(layer_num),
-        _ptr(out["y"]), _ptr(out["groupList"]), _ptr(out["sessionIds"]),
-        _ptr(out["microBatchIds"]), _ptr(out["tokenIds"]), _ptr(out["expertOffsets"]),
-        _ptr(out.get("dynamicScale")), _ptr(out["actualTokenNum"]), _ptr(out.get("sortedIndices")),
-        _ptr(workspace), int(workspace.numel()), _stream(stream, dev))
+    args = [_ptr(expert_ids), int(layer_id), _ptr(token_data), int(token_row_stride), _ptr(scales),
+            int(scale_stride), _ptr(session_ids), _ptr(micro_batch_ids), _ptr(token_ids),
+            int(expert_num), shape, int(token_dtype), int(need_schedule), int(layer_num),
+            _ptr(out["y"]), _ptr(out["groupList"]), _ptr(out["sessionIds"]),
+            _ptr(out["microBatchIds"]), _ptr(out["tokenIds"]), _ptr(out["expertOffsets"]),
+            _ptr(out.get("dynamicScale")), _ptr(out["actualTokenNum"]), _ptr(out.get("sortedIndices"))]
+    tail = [_ptr(workspace), int(workspace.numel()), _stream(stream, dev)]
+    if full_tail:
+        st = lib().ffnwb_batching_ex(*args, MR_BATCHING_FULL_TAIL, *tail)
+    else:
+        st = lib().ffnwb_batching(*args, *tail)
     _check(st, "ffnwb_batching")
     return out
 
@@ -135,10 +140,11 @@ def batching_context_workspace_size(expert_num: int, max_out_shape, token_dtype:
 def ffnwb_batching_context(schedule_context, *, expert_num: int, max_out_shape, token_dtype: int,
                            layer_num: int = 1, need_schedule: int = 0,
                            wait_timeout_us: int = 1_000_000, out: dict | None = None,
-                           workspace=None, stream=None) -> dict:
+                           workspace=None, stream=None, full_tail: bool = False) -> dict:
     """Batching from a ScheduleContext (a CUDA tensor of its 1024 bytes) on the
     current stream. Returns the batching outputs plus scheduleStatus (int32 [1]):
-    blocks not ready with need_schedule = 1, or -1 for a context that does not fit."""
+    blocks not ready with need_schedule = 1, or -1 for a context that does not fit.
+    full_tail: also gather the rows (and ids) of the context's masked slots."""
     _require_cuda("schedule_context", schedule_context)
     if schedule_context.numel() * schedule_context.element_size() < 1024:
         raise ValueError("schedule_context must hold 1024 bytes")
@@ -152,13 +158,16 @@ def ffnwb_batching_context(schedule_context, *, expert_num: int, max_out_shape, 
         ws = batching_context_workspace_size(expert_num, max_out_shape, token_dtype, layer_num,
                                              need_schedule)
         workspace = torch.empty(max(ws, 1), dtype=torch.uint8, device=dev)
-    st = lib().ffnwb_batching_context(
-        _ptr(schedule_context), int(expert_num), int64_array(max_out_shape), int(token_dtype),
-        int(need_schedule), int(layer_num), int(wait_timeout_us), _ptr(out["y"]),
-        _ptr(out["groupList"]), _ptr(out["sessionIds"]), _ptr(out["microBatchIds"]),
-        _ptr(out["tokenIds"]), _ptr(out["expertOffsets"]), _ptr(out.get("dynamicScale")),
-        _ptr(out["actualTokenNum"]), _ptr(out["scheduleStatus"]), _ptr(workspace),
-        int(workspace.numel()), _stream(stream, dev))
+    args = [_ptr(schedule_context), int(expert_num), int64_array(max_out_shape), int(token_dtype),
+            int(need_schedule), int(layer_num), int(wait_timeout_us), _ptr(out["y"]),
+            _ptr(out["groupList"]), _ptr(out["sessionIds"]), _ptr(out["microBatchIds"]),
+            _ptr(out["tokenIds"]), _ptr(out["expertOffsets"]), _ptr(out.get("dynamicScale")),
+            _ptr(out["actualTokenNum"]), _ptr(out["scheduleStatus"])]
+    tail = [_ptr(workspace), int(workspace.numel()), _stream(stream, dev)]
+    if full_tail:
+        st = lib().ffnwb_batching_context_ex(*args, MR_BATCHING_FULL_TAIL, *tail)
+    else:
+        st = lib().ffnwb_batching_context(*args, *tail)
     _check(st, "ffnwb_batching_context")
     return out
 

@@ -15,6 +15,8 @@
 //                      gather_idx (workspace) and the optional slot -> row map
 //   4. row gather    : y rows (and dynamic scales), one warp per row,
 //                      16-byte streaming loads/stores when aligned
+// With MR_BATCHING_FULL_TAIL the scatter and the gather also serve the rows of
+// the masked slots (keys equal to the sentinel): 计算公式 applied to every i.
 #include <cstdio>
 #include <cstdlib>
 
@@ -35,19 +37,26 @@ extern "C" mr_status ffnwb_batching_get_workspace_size(int64_t expertNum, const 
     return MR_OK;
 }
 
-extern "C" mr_status ffnwb_batching(const int32_t* expertIds, int32_t layerId, const void* tokenData,
-                                    int64_t tokenRowStride, const void* scales, int64_t scaleStride,
-                                    const int32_t* sessionIdsIn, const int32_t* microBatchIdsIn,
-                                    const int32_t* tokenIdsIn, int64_t expertNum,
-                                    const int64_t* maxOutShape, int64_t tokenDtype,
-                                    int64_t needSchedule, int64_t layerNum, void* y,
-                                    int64_t* groupList, int32_t* sessionIds, int32_t* microBatchIds,
-                                    int32_t* tokenIds, int32_t* expertOffsets, float* dynamicScale,
-                                    int64_t* actualTokenNum, int32_t* sortedIndicesOut,
-                                    void* workspace, uint64_t workspaceSize, void* stream) {
+extern "C" mr_status ffnwb_batching_ex(const int32_t* expertIds, int32_t layerId,
+                                       const void* tokenData, int64_t tokenRowStride,
+                                       const void* scales, int64_t scaleStride,
+                                       const int32_t* sessionIdsIn, const int32_t* microBatchIdsIn,
+                                       const int32_t* tokenIdsIn, int64_t expertNum,
+                                       const int64_t* maxOutShape, int64_t tokenDtype,
+                                       int64_t needSchedule, int64_t layerNum, void* y,
+                                       int64_t* groupList, int32_t* sessionIds,
+                                       int32_t* microBatchIds, int32_t* tokenIds,
+                                       int32_t* expertOffsets, float* dynamicScale,
+                                       int64_t* actualTokenNum, int32_t* sortedIndicesOut,
+                                       uint32_t flags, void* workspace, uint64_t workspaceSize,
+                                       void* stream) {
     BatchPlan p;
     mr_status st = plan_batching(expertNum, maxOutShape, tokenDtype, needSchedule, layerNum, &p);
     if (st != MR_OK) return st;
+    if (flags & ~(uint32_t)MR_BATCHING_FULL_TAIL) return MR_ERR_PARAM_INVALID;
+    // keys below this bound have a token row to gather: the experts', and the
+    // sentinel's too with the whole-tail option
+    const int row_keys = (int)p.E + ((flags & MR_BATCHING_FULL_TAIL) ? 1 : 0);
     if (!expertIds || !tokenData || !sessionIdsIn || !microBatchIdsIn || !y || !groupList ||
         !sessionIds || !microBatchIds || !tokenIds || !expertOffsets || !actualTokenNum)
         return MR_ERR_PARAM_NULLPTR;
@@ -75,7 +84,7 @@ extern "C" mr_status ffnwb_batching(const int32_t* expertIds, int32_t layerId, c
         const int64_t cap = (int64_t)device_sm_count() * 8;
         const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
         MR_TRY_CUDA(launch_pdl(batching_scatter_kernel<BatchKey>, dim3(grid), dim3(256), 0, s, kf, p.Y, p.B,
-                               cs, sessionIdsIn, microBatchIdsIn, tokenIdsIn, sessionIds,
+                               row_keys, cs, sessionIdsIn, microBatchIdsIn, tokenIdsIn, sessionIds,
                                microBatchIds, tokenIds, expertOffsets, gather_idx,
                                sortedIndicesOut));
     }
@@ -85,8 +94,25 @@ extern "C" mr_status ffnwb_batching(const int32_t* expertIds, int32_t layerId, c
                            reinterpret_cast<const uint8_t*>(tokenData), tokenRowStride,
                            p.row_bytes, int8 ? 1 : 0, reinterpret_cast<const uint8_t*>(scales),
                            scaleStride, reinterpret_cast<uint8_t*>(y), dynamicScale, gather_idx,
-                           cs.bucket_start, (int)p.E, (const uint64_t*)nullptr));
+                           cs.bucket_start, row_keys, (const uint64_t*)nullptr));
     profile_mark(s, 3);
     MR_TRY_CUDA(cudaGetLastError());
     return MR_OK;
+}
+
+extern "C" mr_status ffnwb_batching(const int32_t* expertIds, int32_t layerId, const void* tokenData,
+                                    int64_t tokenRowStride, const void* scales, int64_t scaleStride,
+                                    const int32_t* sessionIdsIn, const int32_t* microBatchIdsIn,
+                                    const int32_t* tokenIdsIn, int64_t expertNum,
+                                    const int64_t* maxOutShape, int64_t tokenDtype,
+                                    int64_t needSchedule, int64_t layerNum, void* y,
+                                    int64_t* groupList, int32_t* sessionIds, int32_t* microBatchIds,
+                                    int32_t* tokenIds, int32_t* expertOffsets, float* dynamicScale,
+                                    int64_t* actualTokenNum, int32_t* sortedIndicesOut,
+                                    void* workspace, uint64_t workspaceSize, void* stream) {
+    return ffnwb_batching_ex(expertIds, layerId, tokenData, tokenRowStride, scales, scaleStride,
+                             sessionIdsIn, microBatchIdsIn, tokenIdsIn, expertNum, maxOutShape,
+                             tokenDtype, needSchedule, layerNum, y, groupList, sessionIds,
+                             microBatchIds, tokenIds, expertOffsets, dynamicScale, actualTokenNum,
+                             sortedIndicesOut, 0u, workspace, workspaceSize, stream);
 }

@@ -27,9 +27,12 @@ struct KeyArray {
     __device__ __forceinline__ int operator()(int64_t s) const { return __ldg(keys + s); }
 };
 
+// Slots with key < kf.E are routed; keys in [kf.E, src_keys) are masked slots
+// that still have a token row (their ids are looked up when the formula is
+// applied to the whole tail); larger keys have no slot behind them.
 template <class KeyFn>
 static __global__ void __launch_bounds__(256)
-batching_scatter_kernel(KeyFn kf, int64_t Y, int B, CsortBufs cs,
+batching_scatter_kernel(KeyFn kf, int64_t Y, int B, int src_keys, CsortBufs cs,
                         const int32_t* __restrict__ sess_in, const int32_t* __restrict__ micro_in,
                         const int32_t* __restrict__ tok_in, int32_t* __restrict__ sess_out,
                         int32_t* __restrict__ micro_out, int32_t* __restrict__ tok_out,
@@ -47,6 +50,12 @@ batching_scatter_kernel(KeyFn kf, int64_t Y, int B, CsortBufs cs,
             tok_out[d] = tok_in ? tok_in[s] : (int32_t)s;
             eoff_out[d] = (int32_t)(d - cs.bucket_start[k]);
             if (slot_row) slot_row[s] = (int32_t)d;
+        } else if (k < src_keys) {
+            sess_out[d] = sess_in[s];
+            micro_out[d] = micro_in[s];
+            tok_out[d] = tok_in ? tok_in[s] : (int32_t)s;
+            eoff_out[d] = -1;
+            if (slot_row) slot_row[s] = -1;
         } else {
             sess_out[d] = -1;
             micro_out[d] = -1;
@@ -171,13 +180,15 @@ batching_gather_kernel(const uint8_t* __restrict__ token_data_arg, int64_t row_s
                        int64_t row_bytes, int is_int8, const uint8_t* __restrict__ scales,
                        int64_t scale_stride, uint8_t* __restrict__ y, float* __restrict__ dyn,
                        const int32_t* __restrict__ gather_idx,
-                       const uint32_t* __restrict__ bucket_start, int E,
+                       const uint32_t* __restrict__ bucket_start, int row_keys,
                        const uint64_t* __restrict__ token_data_loc) {
     pdl_enter();
     // the token rows' address, passed directly or read from device memory
     const uint8_t* __restrict__ token_data =
         token_data_loc ? reinterpret_cast<const uint8_t*>(*token_data_loc) : token_data_arg;
-    const uint32_t U = bucket_start[E];
+    // rows of the keys below row_keys: the routed rows (row_keys = E), or
+    // every row with a token row behind it (the whole-tail option)
+    const uint32_t U = bucket_start[row_keys];
     const int lane = threadIdx.x & 31;
     const bool base16 = (reinterpret_cast<uintptr_t>(token_data) & 15u) == 0u;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;

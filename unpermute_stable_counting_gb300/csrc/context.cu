@@ -119,10 +119,12 @@ context_parse_kernel(const uint8_t* __restrict__ ctx, int64_t Y, int32_t El, int
             micro_ids[g] = m_id;
         }
     }
-    // output rows past the context's slots belong to the masked tail
+    // output rows past the context's slots belong to the masked tail; their
+    // key E + 1 sorts them after the context's masked slots, which (key E)
+    // still have a token row
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t g = v.slots + (int64_t)blockIdx.x * blockDim.x + threadIdx.x; g < Y; g += stride) {
-        keys[g] = E;
+        keys[g] = E + 1;
         sess[g] = 0;
         micro_ids[g] = 0;
     }
@@ -134,6 +136,8 @@ static mr_status plan_context(int64_t expertNum, const int64_t* maxOutShape, int
     if (needSchedule != 0 && needSchedule != 1) return MR_ERR_PARAM_INVALID;
     const mr_status st = plan_batching(expertNum, maxOutShape, tokenDtype, 0, layerNum, p);
     if (st != MR_OK) return st;
+    p->B = (int)p->E + 2;  // experts, the masked sentinel E, and E + 1 for rows with no slot
+    p->ws_bytes = csort_workspace_bytes(p->Y, p->B) + align_up((uint64_t)p->Y * 4u, 256);
     *ws = p->ws_bytes + 3 * align_up((uint64_t)p->Y * 4u, 256);
     return MR_OK;
 }
@@ -158,16 +162,18 @@ extern "C" mr_status ffnwb_batching_context_get_workspace_size(int64_t expertNum
     return MR_OK;
 }
 
-extern "C" mr_status ffnwb_batching_context(
+extern "C" mr_status ffnwb_batching_context_ex(
     const void* scheduleContext, int64_t expertNum, const int64_t* maxOutShape, int64_t tokenDtype,
     int64_t needSchedule, int64_t layerNum, int64_t waitTimeoutUs, void* y, int64_t* groupList,
     int32_t* sessionIds, int32_t* microBatchIds, int32_t* tokenIds, int32_t* expertOffsets,
-    float* dynamicScale, int64_t* actualTokenNum, int32_t* scheduleStatus, void* workspace,
-    uint64_t workspaceSize, void* stream) {
+    float* dynamicScale, int64_t* actualTokenNum, int32_t* scheduleStatus, uint32_t flags,
+    void* workspace, uint64_t workspaceSize, void* stream) {
     BatchPlan p;
     uint64_t ws = 0;
     mr_status st = plan_context(expertNum, maxOutShape, tokenDtype, needSchedule, layerNum, &p, &ws);
     if (st != MR_OK) return st;
+    if (flags & ~(uint32_t)MR_BATCHING_FULL_TAIL) return MR_ERR_PARAM_INVALID;
+    const int row_keys = (int)p.E + ((flags & MR_BATCHING_FULL_TAIL) ? 1 : 0);
     if (!scheduleContext || !y || !groupList || !sessionIds || !microBatchIds || !tokenIds ||
         !expertOffsets || !actualTokenNum)
         return MR_ERR_PARAM_NULLPTR;
@@ -205,7 +211,7 @@ extern "C" mr_status ffnwb_batching_context(
     GroupListOut gl{groupList, actualTokenNum, (int)p.E};
     MR_TRY_CUDA(csort_run(kf, p.Y, p.B, cs, gl, s));
     MR_TRY_CUDA(launch_pdl(batching_scatter_kernel<KeyArray>, dim3(grid), dim3(256), 0, s, kf, p.Y,
-                           p.B, cs, (const int32_t*)sess, (const int32_t*)micro,
+                           p.B, row_keys, cs, (const int32_t*)sess, (const int32_t*)micro,
                            (const int32_t*)nullptr, sessionIds, microBatchIds, tokenIds,
                            expertOffsets, gather_idx, (int32_t*)nullptr));
     profile_mark(s, 1);
@@ -214,9 +220,22 @@ extern "C" mr_status ffnwb_batching_context(
                            (const uint8_t*)nullptr, row_stride, p.row_bytes, int8 ? 1 : 0,
                            (const uint8_t*)nullptr, (int64_t)4, reinterpret_cast<uint8_t*>(y),
                            dynamicScale, (const int32_t*)gather_idx,
-                           (const uint32_t*)cs.bucket_start, (int)p.E,
+                           (const uint32_t*)cs.bucket_start, row_keys,
                            reinterpret_cast<const uint64_t*>(ctx + kCtxTokenDataField)));
     profile_mark(s, 3);
     MR_TRY_CUDA(cudaGetLastError());
     return MR_OK;
+}
+
+extern "C" mr_status ffnwb_batching_context(
+    const void* scheduleContext, int64_t expertNum, const int64_t* maxOutShape, int64_t tokenDtype,
+    int64_t needSchedule, int64_t layerNum, int64_t waitTimeoutUs, void* y, int64_t* groupList,
+    int32_t* sessionIds, int32_t* microBatchIds, int32_t* tokenIds, int32_t* expertOffsets,
+    float* dynamicScale, int64_t* actualTokenNum, int32_t* scheduleStatus, void* workspace,
+    uint64_t workspaceSize, void* stream) {
+    return ffnwb_batching_context_ex(scheduleContext, expertNum, maxOutShape, tokenDtype,
+                                     needSchedule, layerNum, waitTimeoutUs, y, groupList,
+                                     sessionIds, microBatchIds, tokenIds, expertOffsets,
+                                     dynamicScale, actualTokenNum, scheduleStatus, 0u, workspace,
+                                     workspaceSize, stream);
 }

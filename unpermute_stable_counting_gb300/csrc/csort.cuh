@@ -37,7 +37,7 @@ constexpr int kSortWarps = 8;
 constexpr int kSortThreads = kSortWarps * 32;
 constexpr int kSortChunks = 8;  // 32-item chunks per warp
 constexpr int kSortTile = kSortWarps * 32 * kSortChunks;  // 2048 items per tile
-constexpr int kMaxBuckets = 8193;                          // expertNum <= 8192, plus the sentinel
+constexpr int kMaxBuckets = 8194;  // expertNum <= 8192, the sentinel and a no-slot key
 constexpr int kPrefixWarps = 8;                            // keys per prefix block (one per warp)
 constexpr int kPrefixThreads = kPrefixWarps * 32;
 constexpr int kPrefixPrefetch = 4;                         // 32-tile steps loaded together

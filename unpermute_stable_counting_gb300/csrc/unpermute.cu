@@ -470,7 +470,7 @@ static mr_status plan_unpermute(int64_t permutedRows, int64_t hidden, int32_t to
             cap = n / numExperts;
         }
     }
-    if (hasProbs && numExperts > (int64_t)kMaxBuckets - 1) return MR_ERR_INNER;
+    if (hasProbs && numExperts > MR_MAX_EXPERT_NUM) return MR_ERR_INNER;
     if (hasProbs && T * numExperts >= (INT64_C(1) << 40)) return MR_ERR_INNER;
     if (paddedMode && hasProbs && getenv("MR_VERBOSE")) {
         if (topk > numExperts)
