@@ -643,7 +643,9 @@ def run_workload(args):
 
         def call():
             usc.moe_unpermute(perm, sidx, rm, pr_d, padded_mode=bool(u["padded"]), out=out, workspace=ws)
-        phases = (2, 3)
+        # index (probs; with padding also the sort), reduce, and the sort on the
+        # auxiliary stream (not padded)
+        phases = (2, 3) if u["padded"] else (2, 3, 4)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(10)]
     for _ in range(max(args.warmup, 3)):
         call()
