@@ -121,13 +121,32 @@ def test_no_probs_restore_shape(rows_extra):
     check(inp)
 
 
-def test_large_sort_two_passes():
-    """More than 4096 distinct keys: the index sort runs as LSD passes."""
-    inp = w.make_unpermute_topk(T=3000, k=4, Eu=32, H=16, dtype=1, probs_dtype=1, choices=(2, 4),
-                                seed=10)
-    check(inp)
-    p = w.make_unpermute_padded(T=8192, Eu=64, k=2, H=16, dtype=0, probs_dtype=3, mult=9, seed=10)
-    check(p)
+SORT_CASES = {
+    # one counting-sort pass over every key (up to 4096 keys)
+    "one_pass": lambda: w.make_unpermute_topk(T=500, k=8, Eu=32, H=16, dtype=1, probs_dtype=1,
+                                              choices=(2, 8), seed=15),
+    "one_pass_padded": lambda: w.make_unpermute_padded(T=4032, Eu=64, k=2, H=16, dtype=0,
+                                                       probs_dtype=3, mult=9, seed=16),
+    # LSD passes, two and three of them, ragged tile counts
+    "passes_not_padded": lambda: w.make_unpermute_topk(T=1000, k=6, Eu=32, H=16, dtype=1, probs_dtype=1,
+                                                       choices=(2, 6), seed=11),
+    "passes_padded": lambda: w.make_unpermute_padded(T=8192, Eu=64, k=2, H=16, dtype=0,
+                                                     probs_dtype=3, mult=9, seed=10),
+    "passes_wide_not_padded": lambda: w.make_unpermute_topk(T=20000, k=8, Eu=32, H=16, dtype=1,
+                                                            probs_dtype=1, choices=(3, 8), seed=13),
+    "passes_wide_padded": lambda: w.make_unpermute_padded(T=32768, Eu=64, k=2, H=16, dtype=0,
+                                                          probs_dtype=3, mult=7, seed=14),
+    # 32800 tokens x 512 slots: 16.8M rows, 25-bit keys (topK_num at its maximum)
+    "three_passes": lambda: w.make_unpermute_topk(T=32800, k=512, Eu=16, H=8, dtype=1, probs_dtype=1,
+                                                  choices=(1, 2), seed=17),
+}
+
+
+@pytest.mark.parametrize("case", list(SORT_CASES))
+def test_index_sort_paths(case):
+    """The index sort's forms: one counting-sort pass over every key, and two
+    or three LSD passes (keys beyond 2^24 take three)."""
+    check(SORT_CASES[case]())
 
 
 def test_workspace_reuse_and_side_stream():

@@ -7,10 +7,13 @@
 // Launch sequence on the caller's stream (PDL-chained):
 //   not padded, probs : maskedSelect = column bitmasks -> csort prefix ->
 //                       scatter (+ zero tail)
-//   padded, probs     : permuteProbs[i] = probs[sortedIndices[i], i // capacity]
-//   always            : stable sort of sortedIndices (1-3 LSD passes of the
-//                       counting-sort engine) -> outIndex, permuteTokenId;
-//                       padded: per-token row ranges (CSR) from the sorted keys
+//   always            : stable sort of sortedIndices (one pass of the
+//                       counting-sort engine up to 4096 keys, else 2-3 LSD
+//                       passes) -> outIndex, permuteTokenId; padded: the
+//                       per-token row ranges (CSR) are the one pass's key
+//                       starts, or built from the sorted keys
+//   padded, probs     : permuteProbs[i] = probs[sortedIndices[i], i // capacity],
+//                       written by the sort's first scatter
 //   not padded        : the sort runs on the library's auxiliary stream,
 //                       overlapping the gather-reduce (fork/join events)
 //   always            : gather-reduce, one warp per (token, hidden chunk),
@@ -73,22 +76,6 @@ mask_scatter_kernel(const int8_t* __restrict__ map, const uint32_t* __restrict__
     }
 }
 
-// permuteProbs[i] = probs[sortedIndices[i], i // capacity]  (padded, with probs)
-__global__ void __launch_bounds__(256)
-padded_probs_kernel(const int32_t* __restrict__ si, int64_t n, int64_t T, int64_t Eu, int64_t cap,
-                    const uint8_t* __restrict__ probs, int pes, uint8_t* __restrict__ pp) {
-    pdl_enter();
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-        const int32_t v = si[i];
-        if (v >= 0 && v < T) {
-            copy_prob(pp, i, probs, (int64_t)v * Eu + i / cap, pes);
-        } else {
-            zero_prob(pp, i, pes);
-        }
-    }
-}
-
 // ---------------------------------------------------------------------------
 // Stable sort of sortedIndices (LSD passes of the counting-sort engine).
 // Full key: not padded (invalid first) v+1 for 0 <= v < rows, else 0;
@@ -113,13 +100,32 @@ struct RadixKey {
     }
 };
 
+// The padded probs lookup of the first pass (pp != nullptr): it reads the same
+// sortedIndices element as the key.
+struct PaddedProbs {
+    const uint8_t* probs;
+    uint8_t* pp;
+    int64_t Eu, cap;
+    int pes;
+};
+
 __global__ void __launch_bounds__(256)
 radix_scatter_kernel(RadixKey kf, int64_t n, int B, CsortBufs cs, const int32_t* __restrict__ idx_in,
                      uint32_t* __restrict__ keys_out, int32_t* __restrict__ idx_out,
-                     int32_t* __restrict__ out_index, int32_t* __restrict__ ptid, int64_t topk) {
+                     int32_t* __restrict__ out_index, int32_t* __restrict__ ptid, int64_t topk,
+                     PaddedProbs pprobs) {
     pdl_enter();
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        if (pprobs.pp) {
+            // permuteProbs[i] = probs[sortedIndices[i], i // capacity], 0 if invalid
+            const int32_t v = kf.si[i];
+            if (v >= 0 && (int64_t)v < kf.limit) {
+                copy_prob(pprobs.pp, i, pprobs.probs, (int64_t)v * pprobs.Eu + i / pprobs.cap, pprobs.pes);
+            } else {
+                zero_prob(pprobs.pp, i, pprobs.pes);
+            }
+        }
         const uint32_t fk = kf.full(i);
         const int digit = (int)((fk >> kf.shift) & kf.mask);
         const uint32_t d = csort_dest(digit, i, cs, B);
@@ -414,6 +420,7 @@ unpermute_reduce_scalar_kernel(const uint8_t* __restrict__ permuted, int64_t row
 // ---------------------------------------------------------------------------
 
 constexpr int kRadixDigitBits = 12;
+constexpr double kPdlReduceBytes = 1e9;  // see the not-padded launch below
 
 struct UnpermutePlan {
     int64_t rows, H, n, T, Eu, topk, cap;
@@ -494,7 +501,10 @@ static mr_status plan_unpermute(int64_t permutedRows, int64_t hidden, int32_t to
     p->probs = hasProbs != 0;
     p->padded = paddedMode != 0;
 
-    // sort passes
+    // sort passes: one pass of the counting sort over every key up to
+    // 2^kRadixDigitBits keys, else LSD passes of at most that many bits (a
+    // dense histogram of many more keys than a tile's 2048 items costs more
+    // than a second pass)
     const uint64_t range = paddedMode ? (uint64_t)T + 1 : (uint64_t)permutedRows + 1;
     p->key_range = (uint32_t)range;
     if (range <= (UINT64_C(1) << kRadixDigitBits)) {
@@ -542,7 +552,7 @@ static int elementwise_grid(int64_t n) {
 template <int TDT, int PDT, bool HAS_PROBS, bool PADDED>
 static cudaError_t launch_reduce(const UnpermutePlan& p, const uint8_t* permuted,
                                  const int32_t* si, const void* pp, const int32_t* out_index,
-                                 const int32_t* ptr, uint8_t* out, cudaStream_t s) {
+                                 const int32_t* ptr, uint8_t* out, cudaStream_t s, bool pdl) {
     const int64_t row_bytes = p.H * p.es;
     const bool vec_ok = (row_bytes % 16 == 0) && (reinterpret_cast<uintptr_t>(permuted) % 16 == 0) &&
                         (reinterpret_cast<uintptr_t>(out) % 16 == 0);
@@ -565,13 +575,13 @@ static cudaError_t launch_reduce(const UnpermutePlan& p, const uint8_t* permuted
         const int64_t cap = (int64_t)device_sm_count() * bps;
         if (grid > cap) grid = cap;
         if (grid < 1) grid = 1;
-        return launch_pdl(unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED>, dim3((unsigned)grid),
+        return launch_kernel(pdl, unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED>, dim3((unsigned)grid),
                           dim3(256), 0, s, permuted, p.rows, row_bytes, nvec, chunks, si, p.topk, pp,
                           out_index, ptr, p.T, out);
     }
     int64_t threads = p.H < 256 ? (p.H + 31) / 32 * 32 : 256;
     const int64_t gx = p.T < 0x7fffffff ? p.T : 0x7fffffff;
-    return launch_pdl(unpermute_reduce_scalar_kernel<TDT, PDT, HAS_PROBS, PADDED>, dim3((unsigned)gx),
+    return launch_kernel(pdl, unpermute_reduce_scalar_kernel<TDT, PDT, HAS_PROBS, PADDED>, dim3((unsigned)gx),
                       dim3((unsigned)threads), 0, s, permuted, p.rows, p.H, si, p.topk, pp,
                       out_index, ptr, p.T, out);
 }
@@ -579,13 +589,13 @@ static cudaError_t launch_reduce(const UnpermutePlan& p, const uint8_t* permuted
 template <int TDT, int PDT>
 static cudaError_t dispatch_reduce(const UnpermutePlan& p, const uint8_t* permuted,
                                    const int32_t* si, const void* pp, const int32_t* out_index,
-                                   const int32_t* ptr, uint8_t* out, cudaStream_t s) {
+                                   const int32_t* ptr, uint8_t* out, cudaStream_t s, bool pdl) {
     if (p.probs) {
-        return p.padded ? launch_reduce<TDT, PDT, true, true>(p, permuted, si, pp, out_index, ptr, out, s)
-                        : launch_reduce<TDT, PDT, true, false>(p, permuted, si, pp, out_index, ptr, out, s);
+        return p.padded ? launch_reduce<TDT, PDT, true, true>(p, permuted, si, pp, out_index, ptr, out, s, pdl)
+                        : launch_reduce<TDT, PDT, true, false>(p, permuted, si, pp, out_index, ptr, out, s, pdl);
     }
-    return p.padded ? launch_reduce<TDT, PDT, false, true>(p, permuted, si, pp, out_index, ptr, out, s)
-                    : launch_reduce<TDT, PDT, false, false>(p, permuted, si, pp, out_index, ptr, out, s);
+    return p.padded ? launch_reduce<TDT, PDT, false, true>(p, permuted, si, pp, out_index, ptr, out, s, pdl)
+                    : launch_reduce<TDT, PDT, false, false>(p, permuted, si, pp, out_index, ptr, out, s, pdl);
 }
 
 }  // namespace mr
@@ -661,11 +671,7 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
                               (const uint32_t*)bstart, p.T, p.Eu, p.n,
                               reinterpret_cast<const uint8_t*>(probs), p.pes, pp);
         }
-        if (p.probs && p.padded) {
-            return launch_pdl(padded_probs_kernel, dim3(elementwise_grid(p.n)), dim3(256), 0, ss,
-                              sortedIndices, p.n, p.T, p.Eu, p.cap,
-                              reinterpret_cast<const uint8_t*>(probs), p.pes, pp);
-        }
+        // padded with probs: the lookup runs in the sort's first scatter
         return cudaSuccess;
     };
 
@@ -683,7 +689,12 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
     q += align_up((uint64_t)p.n * 4u, 256);
     idx[1] = reinterpret_cast<int32_t*>(q);
     q += align_up((uint64_t)p.n * 4u, 256);
-    int32_t* ptr = p.padded ? reinterpret_cast<int32_t*>(q) : nullptr;
+    // padded: per-token row ranges. One pass: the key starts are exactly that
+    // (key = token, invalid rows in the last bucket); several passes: built
+    // from the sorted keys.
+    int32_t* ptr = !p.padded ? nullptr
+                   : p.passes == 1 ? reinterpret_cast<int32_t*>(cs.bucket_start)
+                                   : reinterpret_cast<int32_t*>(q);
 
     auto launch_sort = [&](cudaStream_t ss) -> cudaError_t {
         const int64_t limit = p.padded ? p.T : p.rows;
@@ -698,15 +709,17 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
             cudaError_t e = csort_run(kf, p.n, B, cs, none, ss);
             if (e != cudaSuccess) return e;
             const bool last = pass == p.passes - 1;
+            PaddedProbs ppr{reinterpret_cast<const uint8_t*>(probs), nullptr, p.Eu, p.cap, p.pes};
+            if (pass == 0 && p.padded && p.probs) ppr.pp = pp;
             e = launch_pdl(radix_scatter_kernel, dim3(elementwise_grid(p.n)), dim3(256), 0, ss, kf,
                            p.n, B, cs, iin, keys[pass & 1], last ? nullptr : idx[pass & 1],
                            last ? outIndex : nullptr, last ? permuteTokenId : nullptr,
-                           p.topk > 0 ? p.topk : (int64_t)1);
+                           p.topk > 0 ? p.topk : (int64_t)1, ppr);
             if (e != cudaSuccess) return e;
             kin = keys[pass & 1];
             iin = idx[pass & 1];
         }
-        if (p.padded) {
+        if (p.padded && p.passes > 1) {
             return launch_pdl(csr_from_keys_kernel, dim3(elementwise_grid(p.n + 1)), dim3(256), 0,
                               ss, kin, p.n, p.T, ptr);
         }
@@ -716,18 +729,18 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
     // ---- gather-reduce --------------------------------------------------------
     const uint8_t* permuted = reinterpret_cast<const uint8_t*>(permutedTokens);
     uint8_t* out = reinterpret_cast<uint8_t*>(unpermutedTokens);
-    auto launch_reduce_any = [&](cudaStream_t ss) -> cudaError_t {
+    auto launch_reduce_any = [&](cudaStream_t ss, bool pdl) -> cudaError_t {
         switch (p.tdt * 4 + p.pdt) {
             case MR_DTYPE_F16 * 4 + MR_DTYPE_F16:
-                return dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss);
+                return dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss, pdl);
             case MR_DTYPE_F16 * 4 + MR_DTYPE_F32:
-                return dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss);
+                return dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss, pdl);
             case MR_DTYPE_BF16 * 4 + MR_DTYPE_BF16:
-                return dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_BF16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss);
+                return dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_BF16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss, pdl);
             case MR_DTYPE_BF16 * 4 + MR_DTYPE_F32:
-                return dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss);
+                return dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss, pdl);
             case MR_DTYPE_F32 * 4 + MR_DTYPE_F32:
-                return dispatch_reduce<MR_DTYPE_F32, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss);
+                return dispatch_reduce<MR_DTYPE_F32, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss, pdl);
         }
         return cudaErrorInvalidValue;
     };
@@ -753,7 +766,15 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
         }
         if (e == cudaSuccess) {
             profile_mark(s, 6);
-            e = launch_reduce_any(s);
+            // Under PDL the persistent reduce takes the SMs while it waits for
+            // the probs, and the concurrent sort then runs on what is left.
+            // A short reduce would end up waiting for the sort at the join,
+            // so it is launched in plain stream order; a long one (here more
+            // than 1 GB of rows, ~150 us) hides the sort either way and keeps
+            // the launch overlap (measured on GB300: top-k T=4096, k=8, H=4096
+            // 75.7 -> 55.6 us; the 2.1 GB round trip 0.989 vs 0.995 ms)
+            const double reduce_bytes = (double)p.T * (double)p.topk * (double)p.H * p.es;
+            e = launch_reduce_any(s, reduce_bytes > kPdlReduceBytes);
             profile_mark(s, 7);
         }
         const cudaError_t ew = ej == cudaSuccess ? cudaStreamWaitEvent(s, ax->join, 0) : ej;
@@ -765,7 +786,7 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
         MR_TRY_CUDA(launch_sort(s));
         profile_mark(s, 5);
         profile_mark(s, 6);
-        e = launch_reduce_any(s);
+        e = launch_reduce_any(s, true);
         MR_TRY_CUDA(e);
         profile_mark(s, 7);
     }
