@@ -559,9 +559,13 @@ def run_workload(args):
         phases = (0,)
     elif name in ("context", "batching"):
         # the round trip's batching alone, from flat arrays or from a
-        # ScheduleContext (256 sessions x 4 micro-batches x 16 tokens x 9)
+        # ScheduleContext (256 sessions x 4 micro-batches x 16 tokens x 9;
+        # --small: 32 sessions, for profiling)
         spec = dict(w.ROUNDTRIP_BATCHING)
+        if args.small:
+            spec.update(A=32, session=32)
         inp = w.make_batching(**spec)
+        n_sessions = spec["A"]
         Y, H, E, dt = inp["Y"], inp["H"], inp["expertNum"], inp["tokenDtype"]
         El = E // max(inp["layerNum"], 1)
         U = int(((inp["expert_ids"] >= 0) & (inp["expert_ids"] < El)).sum())
@@ -572,10 +576,10 @@ def run_workload(args):
         out = usc.batching_outputs(Y, H, E, dt, dev)
         td = g(inp["token_data"])
         if name == "context":
-            info = w.make_token_info(sessions=256, micro=4, mbs=16, sel=9, expert_ids=inp["expert_ids"],
+            info = w.make_token_info(sessions=n_sessions, micro=4, mbs=16, sel=9, expert_ids=inp["expert_ids"],
                                      layer_ids=inp["layer_id"], flags=1)
             info_d = g(info)
-            ctx = w.pack_schedule_context(sessions=256, micro=4, mbs=16, sel=9, expert_num=El,
+            ctx = w.pack_schedule_context(sessions=n_sessions, micro=4, mbs=16, sel=9, expert_num=El,
                                           info_ptr=info_d.data_ptr(), info_size=info.size,
                                           data_ptr=td.data_ptr(), data_size=td.numel())
             ctx_d = g(ctx)
