@@ -408,40 +408,79 @@ def run_ours(args):
     ph = {p: statistics.mean(v) for p, v in phase.items()}
 
     # ---- end to end through host buffers -----------------------------------
+    # Every step copies its inputs from pinned host memory and reads its
+    # results back, through the same public calls. The steps are pipelined the
+    # way a serving loop would run them: two sets of device buffers, the
+    # host->device copy of step i+1 on one stream while step i computes on
+    # another and step i-1's results go back on a third (the host link's two
+    # directions run at once). The timed region spans the first copy in to the
+    # last copy out.
     e2e = None
     if not args.no_e2e:
-        h_out = {n: torch.empty(t.shape, dtype=t.dtype).pin_memory()
+        names_in = ("ids", "td", "sess", "micro", "tok", "rmap", "probs")
+        hosts = dict(ids=h_ids, td=h_td, sess=h_sess, micro=h_micro, tok=h_tok, rmap=h_rmap,
+                     probs=h_probs)
+        dsets = [d, {n: torch.empty_like(d[n]) for n in names_in}]
+        bouts = [bout, usc.batching_outputs(Y, H, E, inp["tokenDtype"], dev, with_sorted_indices=True)]
+        uouts = [uout, usc.unpermute_outputs(T, H, T * k, inp["tokenDtype"], pdt, dev)]
+        bnames = ("groupList", "actualTokenNum", "sessionIds", "microBatchIds", "tokenIds", "expertOffsets")
+        def host_outputs():
+            o = {("u", n): torch.empty(t.shape, dtype=t.dtype).pin_memory()
                  for n, t in uout.items() if t is not None}
-        h_bout = {n: torch.empty(bout[n].shape, dtype=bout[n].dtype).pin_memory()
-                  for n in ("groupList", "actualTokenNum", "sessionIds", "microBatchIds",
-                            "tokenIds", "expertOffsets")}
-        ins = [(d["ids"], h_ids), (d["td"], h_td), (d["sess"], h_sess), (d["micro"], h_micro),
-               (d["tok"], h_tok), (d["rmap"], h_rmap), (d["probs"], h_probs)]
-        h2d = sum(h.numel() * h.element_size() for _, h in ins)
-        outs = [(uout[n], h_out[n]) for n in h_out] + [(bout[n], h_bout[n]) for n in h_bout]
-        d2h = sum(h.numel() * h.element_size() for _, h in outs)
+            o.update({("b", n): torch.empty(bout[n].shape, dtype=bout[n].dtype).pin_memory()
+                      for n in bnames})
+            return o
+        h_outs = [host_outputs(), host_outputs()]
+        h2d = sum(hosts[n].numel() * hosts[n].element_size() for n in names_in)
+        d2h = sum(t.numel() * t.element_size() for t in h_outs[0].values())
+        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_comp = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
+        for e in ev_comp + ev_out:
+            e.record(stream)
 
-        def e2e_step():
-            for dd, hh in ins:
-                dd.copy_(hh, non_blocking=True)
-            step()
-            for dd, hh in outs:
-                hh.copy_(dd, non_blocking=True)
+        def e2e_step(i):
+            j = i % 2
+            dd, bo, uo = dsets[j], bouts[j], uouts[j]
+            with torch.cuda.stream(s_in):
+                s_in.wait_event(ev_comp[j])          # step i-2 no longer reads this set
+                for n in names_in:
+                    dd[n].copy_(hosts[n], non_blocking=True)
+                ev_in[j].record(s_in)
+            stream.wait_event(ev_in[j])
+            stream.wait_event(ev_out[j])              # step i-2's results are home
+            usc.ffnwb_batching(dd["ids"], dd["td"].view(torch.bfloat16).view(Y, H), dd["sess"], dd["micro"],
+                               expert_num=E, max_out_shape=shape, token_dtype=inp["tokenDtype"],
+                               layer_num=inp["layerNum"], layer_id=inp["layer_id"], token_ids=dd["tok"],
+                               with_sorted_indices=True, out=bo, workspace=bws, stream=stream)
+            usc.moe_unpermute(bo["y"], bo["sortedIndices"], dd["rmap"], dd["probs"].view(torch.bfloat16).view(T, k),
+                              padded_mode=False, out=uo, workspace=uws, stream=stream)
+            ev_comp[j].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[j])
+                for (kind, n), hh in h_outs[j].items():
+                    hh.copy_((uo if kind == "u" else bo)[n], non_blocking=True)
+                ev_out[j].record(s_out)
 
-        for _ in range(2):
-            e2e_step()
+        for i in range(2):
+            e2e_step(i)
         torch.cuda.synchronize()
         barrier()
-        n_e2e = max(3, min(args.steps, 10))
+        n_e2e = max(4, min(args.steps, 10))
         e0.record(stream)
-        for _ in range(n_e2e):
-            e2e_step()
-        e1.record(stream)
+        s_in.wait_event(e0)
+        s_out.wait_event(e0)
+        for i in range(n_e2e):
+            e2e_step(i)
+        e1.record(s_out)
         torch.cuda.synchronize()
         e2e_sec = max_over_ranks(e0.elapsed_time(e1) / 1e3 / n_e2e, world, dev)
         e2e = {"value": aggregate_value(ab["total"], world, e2e_sec), "unit": "GB/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_sec * 1e3,
-               "steps": n_e2e}
+               "steps": n_e2e, "pipeline": "double-buffered: copy in of step i+1, compute of step i "
+                                          "and copy out of step i-1 on three streams"}
+        del dsets, bouts, uouts
 
     if world > 1:
         import torch.distributed as dist
