@@ -67,6 +67,8 @@ FUZZ = [
     (8, 128, 9, 256, 40, 2, 1, "zipf", 0.15),          # 9216 slots, int8 row stride H + 4
     (2, 4, 3, 12, 5, 0, 3, "uniform", 1.0),            # every slot masked
     (16, 64, 64, 4096, 16, 1, 16, "zipf", 0.05),       # 65536 slots, 32 tiles
+    (1024, 4, 8, 512, 8, 1, 1, "zipf", 0.1),           # A at its maximum (1024)
+    (1024, 64, 32, 8192, 8, 1, 8, "zipf", 0.05),       # 2.1M slots (1024 tiles), 8192 experts
 ]
 
 

@@ -149,6 +149,17 @@ def test_index_sort_paths(case):
     check(SORT_CASES[case]())
 
 
+@pytest.mark.parametrize("padded", [0, 1])
+def test_maximum_experts(padded):
+    """8192 experts (the most the maskedSelect and padded layouts take)."""
+    if padded:
+        inp = w.make_unpermute_padded(T=8192, Eu=8192, k=2, H=16, dtype=1, probs_dtype=3, mult=3, seed=18)
+    else:
+        inp = w.make_unpermute_topk(T=96, k=8, Eu=8192, H=24, dtype=1, probs_dtype=1, choices=(1, 8),
+                                    seed=18)
+    check(inp)
+
+
 def test_workspace_reuse_and_side_stream():
     import unpermute_stable_counting_gb300 as usc
     a = w.make_unpermute_topk(T=200, k=8, Eu=32, H=64, dtype=1, probs_dtype=1, seed=41)

@@ -210,21 +210,22 @@ def make_unpermute_padded(*, T: int, Eu: int, k: int, H: int, dtype: int, probs_
     step = Eu // k
     routing = np.zeros((T, Eu), dtype=np.int8)
     t = np.arange(T)
-    for j in range(k):
-        routing[t, (mult * t + step * j) % Eu] = 1
+    cols = np.stack([(mult * t + step * j) % Eu for j in range(k)], axis=1)  # [T, k]
+    routing[t[:, None], cols] = 1
     counts = routing.sum(axis=0)
     cap = int(counts.max())
     sorted_idx = np.full(Eu * cap, -1, dtype=np.int32)
-    for e in range(Eu):
-        toks = np.nonzero(routing[:, e])[0]
-        sorted_idx[e * cap:e * cap + len(toks)] = toks
+    e_idx, t_idx = np.nonzero(routing.T)            # expert-major, tokens ascending
+    first = np.searchsorted(e_idx, np.arange(Eu))   # each expert's first pair
+    sorted_idx[e_idx * cap + (np.arange(len(e_idx)) - first[e_idx])] = t_idx
     permuted = normal_rows(Eu * cap, H, dtype, seed)
     probs = None
     if probs_dtype is not None:
-        g = _rng(seed, _TAG_PROBS).exponential(1.0, size=(T, Eu))
-        g = np.where(routing != 0, g, 0.0)
-        p64 = g / g.sum(axis=1, keepdims=True)
-        probs = _to_storage(p64.astype(np.float32), probs_dtype)
+        # Exp(1) draws for the token's k experts only, normalised (Dirichlet(1))
+        g = _rng(seed, _TAG_PROBS).exponential(1.0, size=(T, k))
+        p = np.zeros((T, Eu), dtype=np.float32)
+        p[t[:, None], cols] = (g / g.sum(axis=1, keepdims=True)).astype(np.float32)
+        probs = _to_storage(p, probs_dtype)
     return dict(permuted=permuted, sortedIndices=sorted_idx, routingMap=routing, probs=probs,
                 permutedRows=int(Eu * cap), H=int(H), tokenDtype=int(dtype), n=int(Eu * cap),
                 probsDtype=int(probs_dtype if probs_dtype is not None else dtype), T=int(T),
