@@ -136,6 +136,9 @@ SORT_CASES = {
                                                             probs_dtype=1, choices=(3, 8), seed=13),
     "passes_wide_padded": lambda: w.make_unpermute_padded(T=32768, Eu=64, k=2, H=16, dtype=0,
                                                           probs_dtype=3, mult=7, seed=14),
+    # padded keys beyond 2^22: LSD passes and the CSR kernel
+    "passes_padded_4m": lambda: w.make_unpermute_padded(T=1 << 22, Eu=16, k=1, H=4, dtype=0,
+                                                        probs_dtype=3, mult=5, seed=19),
     # 32800 tokens x 512 slots: 16.8M rows, 25-bit keys (topK_num at its maximum)
     "three_passes": lambda: w.make_unpermute_topk(T=32800, k=512, Eu=16, H=8, dtype=1, probs_dtype=1,
                                                   choices=(1, 2), seed=17),
@@ -144,8 +147,9 @@ SORT_CASES = {
 
 @pytest.mark.parametrize("case", list(SORT_CASES))
 def test_index_sort_paths(case):
-    """The index sort's forms: one counting-sort pass over every key, and two
-    or three LSD passes (keys beyond 2^24 take three)."""
+    """The index sort's forms: one counting-sort pass over every key; padded,
+    a coarse pass on the high bits and a per-bucket fine sort that writes the
+    row pointers; and two or three LSD passes (keys beyond 2^24 take three)."""
     check(SORT_CASES[case]())
 
 
@@ -157,6 +161,21 @@ def test_maximum_experts(padded):
     else:
         inp = w.make_unpermute_topk(T=96, k=8, Eu=8192, H=24, dtype=1, probs_dtype=1, choices=(1, 8),
                                     seed=18)
+    check(inp)
+
+
+@pytest.mark.parametrize("T,Eu", [(8192, 64), (16384, 128)])
+def test_padded_invalid_rows_and_duplicates(T, Eu):
+    """Two-level padded sort with 40% invalid rows (-1 and >= T: one fine
+    bucket of thousands of rows, many 256-row chunks) and repeated tokens."""
+    inp = w.make_unpermute_padded(T=T, Eu=Eu, k=2, H=24, dtype=1, probs_dtype=3, mult=3, seed=20)
+    rng = np.random.default_rng(T)
+    si = inp["sortedIndices"].copy()
+    bad = rng.random(si.size) < 0.4
+    si[bad] = np.where(rng.random(bad.sum()) < 0.5, -1, T + 7).astype(np.int32)
+    dup = rng.random(si.size) < 0.1
+    si[dup & ~bad] = 5                       # token 5 many times over
+    inp = dict(inp, sortedIndices=si)
     check(inp)
 
 

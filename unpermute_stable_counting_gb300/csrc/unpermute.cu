@@ -109,14 +109,20 @@ struct PaddedProbs {
     int pes;
 };
 
-__global__ void __launch_bounds__(256)
-radix_scatter_kernel(RadixKey kf, int64_t n, int B, CsortBufs cs, const int32_t* __restrict__ idx_in,
-                     uint32_t* __restrict__ keys_out, int32_t* __restrict__ idx_out,
-                     int32_t* __restrict__ out_index, int32_t* __restrict__ ptid, int64_t topk,
-                     PaddedProbs pprobs) {
-    pdl_enter();
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+// The scatter step of one sort pass for item i at position d: the full key
+// and the item's original index move to d (every pass but the last); the last
+// pass writes outIndex and permuteTokenId instead. The first pass of a padded
+// sort with probs also writes permuteProbs[i].
+struct RadixScatter {
+    RadixKey kf;
+    const int32_t* idx_in;
+    uint32_t* keys_out;
+    int32_t* idx_out;
+    int32_t* out_index;
+    int32_t* ptid;
+    int64_t topk;
+    PaddedProbs pprobs;
+    __device__ __forceinline__ void operator()(int64_t i, int, uint32_t d, uint32_t) const {
         if (pprobs.pp) {
             // permuteProbs[i] = probs[sortedIndices[i], i // capacity], 0 if invalid
             const int32_t v = kf.si[i];
@@ -127,8 +133,6 @@ radix_scatter_kernel(RadixKey kf, int64_t n, int B, CsortBufs cs, const int32_t*
             }
         }
         const uint32_t fk = kf.full(i);
-        const int digit = (int)((fk >> kf.shift) & kf.mask);
-        const uint32_t d = csort_dest(digit, i, cs, B);
         const int32_t idx = idx_in ? idx_in[i] : (int32_t)i;
         keys_out[d] = fk;
         if (out_index) {
@@ -137,6 +141,87 @@ radix_scatter_kernel(RadixKey kf, int64_t n, int B, CsortBufs cs, const int32_t*
         } else {
             idx_out[d] = idx;
         }
+    }
+};
+
+__global__ void __launch_bounds__(256)
+radix_scatter_kernel(RadixKey kf, int64_t n, int B, CsortBufs cs, RadixScatter sc) {
+    pdl_enter();
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+        const int digit = kf(i);
+        sc(i, digit, csort_dest(digit, i, cs, B), 0u);
+    }
+}
+
+// Second level of the padded sort (one block per coarse bucket). The first
+// level is a counting-sort pass on key >> s, which leaves each coarse bucket
+// [cstart[c], cstart[c+1]) in original order. The block sorts its bucket
+// stably by the low s bits (F = 2^s fine keys): a histogram and its scan give
+// the fine starts -- which are the CSR row pointers ptr[c*F + f] -- and
+// 256-item chunks taken in order are ranked by key with warp matches, per-warp
+// counters and a running count per fine key.
+constexpr int kFineThreads = 256;
+constexpr int kFineWarps = kFineThreads / 32;
+constexpr int kMaxFineBits = 10;
+
+__global__ void __launch_bounds__(kFineThreads)
+fine_sort_csr_kernel(const uint32_t* __restrict__ keys, const int32_t* __restrict__ idx,
+                     const uint32_t* __restrict__ cstart, int shift, int64_t T,
+                     const int32_t* __restrict__ si, int32_t* __restrict__ out_index,
+                     int32_t* __restrict__ ptid, int32_t* __restrict__ ptr) {
+    extern __shared__ __align__(16) uint32_t fsm[];
+    const int F = 1 << shift;
+    uint32_t* hist = fsm;                     // [F] counts, then fine starts
+    uint32_t* running = fsm + F;              // [F] items placed so far
+    uint32_t* wcnt = fsm + 2 * F;             // [kFineWarps][F] this chunk's counts
+    pdl_enter();
+    const int c = blockIdx.x;
+    const uint32_t lo = cstart[c], hi = cstart[c + 1];
+    const int warp = threadIdx.x >> 5;
+    const uint32_t fmask = (uint32_t)F - 1u;
+    for (int i = threadIdx.x; i < (2 + kFineWarps) * F; i += kFineThreads) fsm[i] = 0u;
+    __syncthreads();
+    for (uint32_t i = lo + threadIdx.x; i < hi; i += kFineThreads) atomicAdd(&hist[keys[i] & fmask], 1u);
+    __syncthreads();
+    if (threadIdx.x == 0) {  // F <= 1024 counts: a serial scan is a few hundred cycles
+        uint32_t run = 0u;
+        for (int f = 0; f < F; ++f) {
+            const uint32_t h = hist[f];
+            hist[f] = run;
+            run += h;
+        }
+    }
+    __syncthreads();
+    // row pointers of the tokens in this coarse bucket (key T: the invalid rows)
+    for (int f = threadIdx.x; f < F; f += kFineThreads) {
+        const int64_t t = (int64_t)c * F + f;
+        if (t <= T) ptr[t] = (int32_t)(lo + hist[f]);
+    }
+    const uint32_t lt = lanemask_lt();
+    for (uint32_t base = lo; base < hi; base += kFineThreads) {
+        const uint32_t i = base + threadIdx.x;
+        const bool in = i < hi;
+        const int f = in ? (int)(keys[i] & fmask) : -1;
+        const uint32_t peers = __match_any_sync(0xffffffffu, f);
+        const uint32_t below = __popc(peers & lt);
+        const bool leader = in && below == 0u;
+        if (leader) wcnt[warp * F + f] = __popc(peers);
+        __syncthreads();
+        if (in) {
+            uint32_t r = below + running[f] + hist[f];
+            for (int w = 0; w < warp; ++w) r += wcnt[w * F + f];
+            const uint32_t pos = lo + r;
+            const int32_t o = idx[i];
+            out_index[pos] = o;
+            ptid[pos] = si[o];
+        }
+        __syncthreads();
+        if (leader) {
+            atomicAdd(&running[f], (uint32_t)__popc(peers));
+            wcnt[warp * F + f] = 0u;
+        }
+        __syncthreads();
     }
 }
 
@@ -428,6 +513,8 @@ struct UnpermutePlan {
     bool probs, padded;
     // sort
     uint32_t key_range;  // number of distinct full keys
+    int fine_bits;       // padded beyond one pass: a pass on key >> fine_bits, then
+                         // fine_sort_csr_kernel (0: LSD passes or one pass)
     int passes;
     int shift[3];
     int bits[3];
@@ -507,7 +594,20 @@ static mr_status plan_unpermute(int64_t permutedRows, int64_t hidden, int32_t to
     // than a second pass)
     const uint64_t range = paddedMode ? (uint64_t)T + 1 : (uint64_t)permutedRows + 1;
     p->key_range = (uint32_t)range;
-    if (range <= (UINT64_C(1) << kRadixDigitBits)) {
+    p->fine_bits = 0;
+    if (paddedMode && range > (UINT64_C(1) << kRadixDigitBits) &&
+        range <= (UINT64_C(1) << (kRadixDigitBits + kMaxFineBits))) {
+        // padded: coarse counting sort on key >> s (257..4096 buckets), then
+        // one block per coarse bucket sorts by the low s bits and writes the CSR;
+        // s leaves about 2^9 coarse buckets while the fine keys fit a block
+        const int b = bits_for(range);
+        const int sbits = b - 9 < kMaxFineBits ? b - 9 : kMaxFineBits;
+        p->fine_bits = sbits;
+        p->passes = 1;
+        p->shift[0] = sbits;
+        p->bits[0] = kRadixDigitBits;
+        p->Bmax = (int)(((range - 1) >> sbits) + 1);
+    } else if (range <= (UINT64_C(1) << kRadixDigitBits)) {
         p->passes = 1;
         p->shift[0] = 0;
         p->bits[0] = bits_for(range);
@@ -534,7 +634,7 @@ static mr_status plan_unpermute(int64_t permutedRows, int64_t hidden, int32_t to
         ms = align_up(items * 4u, 256) * 2 + align_up((uint64_t)numExperts * 4u, 256) +
              align_up((uint64_t)(numExperts + 1) * 4u, 256) + 256;
     }
-    const int Bsort = p->passes == 1 ? (int)range : p->Bmax;
+    const int Bsort = p->fine_bits ? p->Bmax : p->passes == 1 ? (int)range : p->Bmax;
     uint64_t sb = csort_workspace_bytes(n, Bsort) + 4 * align_up((uint64_t)n * 4u, 256);
     if (paddedMode) sb += align_up((uint64_t)(T + 1) * 4u, 256);
     p->ms_bytes = ms;
@@ -677,7 +777,7 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
 
     // ---- stable sort of sortedIndices -> outIndex, permuteTokenId ----------
     uint8_t* q = wp + p.ms_bytes;
-    const int Bsort = p.passes == 1 ? (int)p.key_range : p.Bmax;
+    const int Bsort = p.fine_bits ? p.Bmax : p.passes == 1 ? (int)p.key_range : p.Bmax;
     CsortBufs cs = csort_carve(q, p.n, Bsort);
     uint32_t* keys[2];
     int32_t* idx[2];
@@ -693,31 +793,43 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
     // (key = token, invalid rows in the last bucket); several passes: built
     // from the sorted keys.
     int32_t* ptr = !p.padded ? nullptr
-                   : p.passes == 1 ? reinterpret_cast<int32_t*>(cs.bucket_start)
-                                   : reinterpret_cast<int32_t*>(q);
+                   : (p.passes == 1 && !p.fine_bits) ? reinterpret_cast<int32_t*>(cs.bucket_start)
+                                                     : reinterpret_cast<int32_t*>(q);
 
     auto launch_sort = [&](cudaStream_t ss) -> cudaError_t {
         const int64_t limit = p.padded ? p.T : p.rows;
         const uint32_t* kin = nullptr;
         const int32_t* iin = nullptr;
         for (int pass = 0; pass < p.passes; ++pass) {
-            const int B = p.passes == 1 ? (int)p.key_range : (1 << p.bits[pass]);
-            const uint32_t mask =
-                p.passes == 1 ? 0xffffffffu : (uint32_t)((1u << p.bits[pass]) - 1u);
+            const int B = p.fine_bits ? p.Bmax : p.passes == 1 ? (int)p.key_range : (1 << p.bits[pass]);
+            const uint32_t mask = (p.passes == 1 || p.fine_bits)
+                                      ? 0xffffffffu : (uint32_t)((1u << p.bits[pass]) - 1u);
             RadixKey kf{sortedIndices, kin, limit, p.padded ? 1 : 0, p.shift[pass], mask};
             GroupListOut none{nullptr, nullptr, 0};
-            cudaError_t e = csort_run(kf, p.n, B, cs, none, ss);
-            if (e != cudaSuccess) return e;
-            const bool last = pass == p.passes - 1;
+            const bool last = pass == p.passes - 1 && !p.fine_bits;
             PaddedProbs ppr{reinterpret_cast<const uint8_t*>(probs), nullptr, p.Eu, p.cap, p.pes};
             if (pass == 0 && p.padded && p.probs) ppr.pp = pp;
-            e = launch_pdl(radix_scatter_kernel, dim3(elementwise_grid(p.n)), dim3(256), 0, ss, kf,
-                           p.n, B, cs, iin, keys[pass & 1], last ? nullptr : idx[pass & 1],
-                           last ? outIndex : nullptr, last ? permuteTokenId : nullptr,
-                           p.topk > 0 ? p.topk : (int64_t)1, ppr);
+            RadixScatter sc{kf, iin, keys[pass & 1], last ? nullptr : idx[pass & 1],
+                            last ? outIndex : nullptr, last ? permuteTokenId : nullptr,
+                            p.topk > 0 ? p.topk : (int64_t)1, ppr};
+            cudaError_t e = csort_run(kf, p.n, B, cs, none, ss);
+            if (e != cudaSuccess) return e;
+            e = launch_pdl(radix_scatter_kernel, dim3(elementwise_grid(p.n)), dim3(256), 0, ss, kf, p.n, B,
+                           cs, sc);
             if (e != cudaSuccess) return e;
             kin = keys[pass & 1];
             iin = idx[pass & 1];
+        }
+        if (p.fine_bits) {
+            const size_t smem = (size_t)(2 + kFineWarps) * ((size_t)1 << p.fine_bits) * 4u;
+            if (smem > 48 * 1024) {
+                cudaError_t e = cudaFuncSetAttribute(fine_sort_csr_kernel,
+                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                if (e != cudaSuccess) return e;
+            }
+            return launch_pdl(fine_sort_csr_kernel, dim3((unsigned)p.Bmax), dim3(kFineThreads), smem, ss,
+                              (const uint32_t*)kin, (const int32_t*)iin, (const uint32_t*)cs.bucket_start,
+                              p.fine_bits, p.T, sortedIndices, outIndex, permuteTokenId, ptr);
         }
         if (p.padded && p.passes > 1) {
             return launch_pdl(csr_from_keys_kernel, dim3(elementwise_grid(p.n + 1)), dim3(256), 0,
