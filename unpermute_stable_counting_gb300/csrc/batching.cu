@@ -78,16 +78,9 @@ extern "C" mr_status ffnwb_batching_ex(const int32_t* expertIds, int32_t layerId
     GroupListOut gl{groupList, actualTokenNum, (int)p.E};
 
     profile_mark(s, 0);
-    MR_TRY_CUDA(csort_run(kf, p.Y, p.B, cs, gl, s));
-    {
-        const int64_t want = (p.Y + 255) / 256;
-        const int64_t cap = (int64_t)device_sm_count() * 8;
-        const int grid = (int)(want < cap ? (want > 0 ? want : 1) : cap);
-        MR_TRY_CUDA(launch_pdl(batching_scatter_kernel<BatchKey>, dim3(grid), dim3(256), 0, s, kf, p.Y, p.B,
-                               row_keys, cs, sessionIdsIn, microBatchIdsIn, tokenIdsIn, sessionIds,
-                               microBatchIds, tokenIds, expertOffsets, gather_idx,
-                               sortedIndicesOut));
-    }
+    BatchScatter<BatchKey> sc{kf, row_keys, sessionIdsIn, microBatchIdsIn, tokenIdsIn, sessionIds,
+                              microBatchIds, tokenIds, expertOffsets, gather_idx, sortedIndicesOut};
+    MR_TRY_CUDA(batching_index(kf, p.Y, p.B, cs, gl, sc, s));
     profile_mark(s, 1);
     profile_mark(s, 2);
     MR_TRY_CUDA(launch_pdl(batching_gather_kernel<7>, dim3(gather_grid(p.Y)), dim3(256), 0, s,

@@ -209,11 +209,9 @@ extern "C" mr_status ffnwb_batching_context_ex(
                            scheduleStatus));
     KeyArray kf{keys, (int32_t)p.E};
     GroupListOut gl{groupList, actualTokenNum, (int)p.E};
-    MR_TRY_CUDA(csort_run(kf, p.Y, p.B, cs, gl, s));
-    MR_TRY_CUDA(launch_pdl(batching_scatter_kernel<KeyArray>, dim3(grid), dim3(256), 0, s, kf, p.Y,
-                           p.B, row_keys, cs, (const int32_t*)sess, (const int32_t*)micro,
-                           (const int32_t*)nullptr, sessionIds, microBatchIds, tokenIds,
-                           expertOffsets, gather_idx, (int32_t*)nullptr));
+    BatchScatter<KeyArray> sc{kf, row_keys, sess, micro, nullptr, sessionIds, microBatchIds, tokenIds,
+                              expertOffsets, gather_idx, nullptr};
+    MR_TRY_CUDA(batching_index(kf, p.Y, p.B, cs, gl, sc, s));
     profile_mark(s, 1);
     profile_mark(s, 2);
     MR_TRY_CUDA(launch_pdl(batching_gather_kernel<7>, dim3(gather_grid(p.Y)), dim3(256), 0, s,

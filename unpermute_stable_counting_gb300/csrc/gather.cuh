@@ -1,0 +1,169 @@
+// The batching's row gather ("aclnnFfnWorkerBatching", 计算公式 y[i] =
+// token_data[gather_idx[i]], and the INT8 dynamic scale of step 3), kept
+// apart from the index work so that its source is one file.
+#pragma once
+
+#include "common.cuh"
+
+namespace mr {
+
+// 16-byte output vectors from a source that is only 4-byte aligned (INT8 rows
+// with their trailing scale have a stride of H + 4 bytes). With o = src % 16
+// (4, 8 or 12) and `win` the aligned address src - o, output vector j is the
+// tail of window j followed by the head of window j + 1. Lane l loads window
+// j = j0 + l and takes window j + 1 from lane l + 1 by a shuffle. Windows up to
+// nvec - 1 lie inside [win, src + bytes); the last output vector is read as
+// words. The caller uses this only when the buffer base is 16-byte aligned,
+// so win never precedes the buffer.
+constexpr int kShiftVPT = 4;
+
+__device__ __forceinline__ uint4 shift_combine(const uint4& a, const uint4& b, int o) {
+    if (o == 4) return make_uint4(a.y, a.z, a.w, b.x);
+    if (o == 8) return make_uint4(a.z, a.w, b.x, b.y);
+    return make_uint4(a.w, b.x, b.y, b.z);
+}
+
+__device__ __forceinline__ void warp_copy_row_shift(const uint8_t* __restrict__ src,
+                                                    uint8_t* __restrict__ dst, int64_t bytes,
+                                                    int lane) {
+    const int o = (int)(reinterpret_cast<uintptr_t>(src) & 15u);
+    const uint4* win = reinterpret_cast<const uint4*>(src - o);
+    const int nv1 = (int)(bytes >> 4) - 1;  // vectors built from two windows
+    for (int j0 = 0; j0 < nv1; j0 += 32 * kShiftVPT) {
+        uint4 a[kShiftVPT];
+#pragma unroll
+        for (int u = 0; u < kShiftVPT; ++u) {
+            const int j = j0 + 32 * u + lane;
+            a[u] = j <= nv1 ? ld_stream_v4(win + j) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        // lane 31's next window: lane 0's window of the next u, or one more load
+        const int jl = j0 + 32 * (kShiftVPT - 1) + 31;
+        const uint4 extra = (lane == 31 && jl < nv1) ? ld_stream_v4(win + jl + 1)
+                                                     : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int u = 0; u < kShiftVPT; ++u) {
+            const int j = j0 + 32 * u + lane;
+            uint4 b;
+            b.x = __shfl_down_sync(0xffffffffu, a[u].x, 1);
+            b.y = __shfl_down_sync(0xffffffffu, a[u].y, 1);
+            b.z = __shfl_down_sync(0xffffffffu, a[u].z, 1);
+            b.w = __shfl_down_sync(0xffffffffu, a[u].w, 1);
+            if (u + 1 < kShiftVPT) {
+                const uint4 nx = make_uint4(__shfl_sync(0xffffffffu, a[u + 1 < kShiftVPT ? u + 1 : u].x, 0),
+                                            __shfl_sync(0xffffffffu, a[u + 1 < kShiftVPT ? u + 1 : u].y, 0),
+                                            __shfl_sync(0xffffffffu, a[u + 1 < kShiftVPT ? u + 1 : u].z, 0),
+                                            __shfl_sync(0xffffffffu, a[u + 1 < kShiftVPT ? u + 1 : u].w, 0));
+                if (lane == 31) b = nx;
+            } else if (lane == 31) {
+                b = extra;
+            }
+            if (j < nv1) st_stream_v4(dst + 16 * (int64_t)j, shift_combine(a[u], b, o));
+        }
+    }
+    if (lane == 0 && nv1 >= 0) {
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(src + 16 * (int64_t)nv1);
+        st_stream_v4(dst + 16 * (int64_t)nv1, make_uint4(w[0], w[1], w[2], w[3]));
+    }
+}
+
+// Copy `bytes` from src to dst with one warp. Vector width follows the common
+// alignment of both addresses and the length: 16-byte vectors (VPT in flight
+// per lane), else 4-byte words, else bytes. Addresses are formed from the
+// __restrict__ row pointers directly, which leaves the compiler free to start
+// the next batch's loads before the current stores (measured on GB300: 616 us
+// against 626 us for the round-trip gather with pointer casts).
+template <int VPT>
+__device__ __forceinline__ void warp_copy_row(const uint8_t* __restrict__ src,
+                                              uint8_t* __restrict__ dst, int64_t bytes, int lane,
+                                              bool base16) {
+    const uintptr_t mis = (reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst) |
+                           (uintptr_t)bytes);
+    if ((mis & 15u) == 0u) {
+        const int64_t nv = bytes >> 4;
+        int64_t v = lane;
+        for (; v + 32 * (VPT - 1) < nv; v += 32 * VPT) {
+            uint4 r[VPT];
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) r[u] = ld_stream_v4(src + 16 * (v + 32 * u));
+#pragma unroll
+            for (int u = 0; u < VPT; ++u) st_stream_v4(dst + 16 * (v + 32 * u), r[u]);
+        }
+        uint4 r[VPT];
+#pragma unroll
+        for (int u = 0; u < VPT; ++u)
+            if (v + 32 * u < nv) r[u] = ld_stream_v4(src + 16 * (v + 32 * u));
+#pragma unroll
+        for (int u = 0; u < VPT; ++u)
+            if (v + 32 * u < nv) st_stream_v4(dst + 16 * (v + 32 * u), r[u]);
+    } else if (base16 && ((reinterpret_cast<uintptr_t>(dst) | (uintptr_t)bytes) & 15u) == 0u &&
+               (reinterpret_cast<uintptr_t>(src) & 3u) == 0u) {
+        warp_copy_row_shift(src, dst, bytes, lane);
+    } else if ((mis & 3u) == 0u) {
+        constexpr int W = VPT * 4;
+        const int64_t nw = bytes >> 2;
+        int64_t v = lane;
+        for (; v + 32 * (W - 1) < nw; v += 32 * W) {
+            uint32_t r[W];
+#pragma unroll
+            for (int u = 0; u < W; ++u) r[u] = ld_stream_u32(src + 4 * (v + 32 * u));
+#pragma unroll
+            for (int u = 0; u < W; ++u) st_stream_u32(dst + 4 * (v + 32 * u), r[u]);
+        }
+        for (; v < nw; v += 32) st_stream_u32(dst + 4 * v, ld_stream_u32(src + 4 * v));
+    } else {
+        for (int64_t b = lane; b < bytes; b += 32) dst[b] = src[b];
+    }
+}
+
+template <int VPT>
+static __global__ void __launch_bounds__(256)
+batching_gather_kernel(const uint8_t* __restrict__ token_data_arg, int64_t row_stride,
+                       int64_t row_bytes, int is_int8, const uint8_t* __restrict__ scales,
+                       int64_t scale_stride, uint8_t* __restrict__ y, float* __restrict__ dyn,
+                       const int32_t* __restrict__ gather_idx,
+                       const uint32_t* __restrict__ bucket_start, int row_keys,
+                       const uint64_t* __restrict__ token_data_loc) {
+    pdl_enter();
+    // the token rows' address, passed directly or read from device memory
+    const uint8_t* __restrict__ token_data =
+        token_data_loc ? reinterpret_cast<const uint8_t*>(*token_data_loc) : token_data_arg;
+    // rows of the keys below row_keys: the routed rows (row_keys = E), or
+    // every row with a token row behind it (the whole-tail option)
+    const uint32_t U = bucket_start[row_keys];
+    const int lane = threadIdx.x & 31;
+    const bool base16 = (reinterpret_cast<uintptr_t>(token_data) & 15u) == 0u;
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t i = gw; i < (int64_t)U; i += nw) {
+        const int64_t g = gather_idx[i];
+        warp_copy_row<VPT>(token_data + g * row_stride, y + i * row_bytes, row_bytes, lane, base16);
+        if (is_int8) {
+            const uint8_t* sp = scales ? scales + g * scale_stride : token_data + g * row_stride + row_bytes;
+            if ((reinterpret_cast<uintptr_t>(sp) & 3u) == 0u) {
+                if (lane == 0) dyn[i] = *reinterpret_cast<const float*>(sp);
+            } else if (lane < 4) {
+                // an unaligned scale: one byte per lane
+                reinterpret_cast<uint8_t*>(dyn + i)[lane] = sp[lane];
+            }
+        }
+    }
+}
+
+static inline int gather_grid(int64_t rows) {
+    static int blocks_per_sm[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int bps = dev < 64 ? blocks_per_sm[dev] : 0;
+    if (bps == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, batching_gather_kernel<7>, 256, 0) !=
+                cudaSuccess || bps <= 0)
+            bps = 4;
+        if (dev < 64) blocks_per_sm[dev] = bps;
+    }
+    const int64_t want = (rows + 7) / 8;  // 8 warps per block, one row per warp
+    const int64_t cap = (int64_t)device_sm_count() * bps;
+    int64_t g = want < cap ? want : cap;
+    return (int)(g > 0 ? g : 1);
+}
+
+}  // namespace mr

@@ -23,19 +23,10 @@
 #include <cstdlib>
 #include <mutex>
 
+#include "reduce.cuh"
 #include "routing.cuh"
 
 namespace mr {
-
-template <int DT>
-__device__ __forceinline__ float ld_f32(const void* base, int64_t i) {
-    if constexpr (DT == MR_DTYPE_F32) {
-        return __ldg(reinterpret_cast<const float*>(base) + i);
-    } else {
-        const uint16_t b = __ldg(reinterpret_cast<const unsigned short*>(base) + i);
-        return Elem<DT>::to_f32(b);
-    }
-}
 
 // Copy one element of 2 or 4 bytes (the probs dtype) without interpreting it.
 __device__ __forceinline__ void copy_prob(uint8_t* dst, int64_t di, const uint8_t* src, int64_t si,
@@ -236,267 +227,6 @@ csr_from_keys_kernel(const uint32_t* __restrict__ keys, int64_t n, int64_t T,
         const int64_t cur = p < n ? (int64_t)keys[p] : T + 1;
         const int64_t hi = cur < T ? cur : T;
         for (int64_t t = prev + 1; t <= hi; ++t) ptr[t] = (int32_t)p;
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Gather-reduce. A token's contributing rows are those with a valid index
-// and, with probs, a nonzero prob, taken in ascending slot (not padded) or
-// row (padded) order; they are added in fp32, acc = acc + f32(x) * f32(p),
-// each operation rounded on its own, then cast once with RNE.
-// ---------------------------------------------------------------------------
-constexpr int kListCap = 512;   // list entries per pass of the element-wise kernel
-constexpr int kRedUnroll = 4;   // rows in flight per warp step
-constexpr int kRedVQ = 2;       // 16-byte vectors per lane per work item
-
-template <bool HAS_PROBS, bool PADDED, int PDT>
-__device__ __forceinline__ int build_list(int64_t c0, int64_t c1, const int32_t* __restrict__ si,
-                                          int64_t rows, int64_t row_bytes,
-                                          const void* __restrict__ pp,
-                                          const int32_t* __restrict__ out_index, int64_t* s_row,
-                                          float* s_w) {
-    const int lane = threadIdx.x & 31;
-    int cnt = 0;
-    for (int64_t e0 = c0; e0 < c1; e0 += 32) {
-        const int64_t e = e0 + lane;
-        bool keep = false;
-        int64_t r = 0;
-        float w = 1.0f;
-        if (e < c1) {
-            if (PADDED) {
-                r = out_index[e];
-                keep = true;
-            } else {
-                const int32_t v = si[e];
-                keep = v >= 0 && (int64_t)v < rows;
-                r = v;
-            }
-            if (HAS_PROBS && keep) {
-                w = ld_f32<PDT>(pp, PADDED ? r : e);
-                keep = w != 0.0f;
-            }
-        }
-        const uint32_t bal = __ballot_sync(0xffffffffu, keep);
-        if (keep) {
-            const int pos = cnt + __popc(bal & lanemask_lt());
-            s_row[pos] = r * row_bytes;
-            s_w[pos] = w;
-        }
-        cnt += __popc(bal);
-    }
-    return cnt;
-}
-
-template <int TDT>
-struct Vec;
-template <>
-struct Vec<MR_DTYPE_F32> {
-    static constexpr int N = 4;
-    static __device__ __forceinline__ void unpack(const uint4& v, float* x) {
-        x[0] = __uint_as_float(v.x);
-        x[1] = __uint_as_float(v.y);
-        x[2] = __uint_as_float(v.z);
-        x[3] = __uint_as_float(v.w);
-    }
-    static __device__ __forceinline__ uint4 pack(const float* a) {
-        return make_uint4(__float_as_uint(a[0]), __float_as_uint(a[1]), __float_as_uint(a[2]),
-                          __float_as_uint(a[3]));
-    }
-};
-template <int DT>
-struct Vec16 {
-    static constexpr int N = 8;
-    static __device__ __forceinline__ void unpack(const uint4& v, float* x) {
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            x[2 * k] = Elem<DT>::to_f32((uint16_t)(w[k] & 0xffffu));
-            x[2 * k + 1] = Elem<DT>::to_f32((uint16_t)(w[k] >> 16));
-        }
-    }
-    static __device__ __forceinline__ uint4 pack(const float* a) {
-        uint32_t w[4];
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            w[k] = (uint32_t)Elem<DT>::from_f32(a[2 * k]) |
-                   ((uint32_t)Elem<DT>::from_f32(a[2 * k + 1]) << 16);
-        return make_uint4(w[0], w[1], w[2], w[3]);
-    }
-};
-template <>
-struct Vec<MR_DTYPE_F16> : Vec16<MR_DTYPE_F16> {};
-template <>
-struct Vec<MR_DTYPE_BF16> : Vec16<MR_DTYPE_BF16> {};
-
-// One warp per work item = (token, chunk of 32*kRedVQ 16-byte vectors of the
-// hidden dimension). The warp's lanes load up to 32 of the token's slots at a
-// time (index and weight), a ballot keeps the contributing ones in ascending
-// order, and the warp adds them kRedUnroll rows at a time, each lane owning
-// kRedVQ vectors: no shared memory and no block barrier.
-template <int TDT, int PDT, bool HAS_PROBS, bool PADDED>
-__global__ void __launch_bounds__(256)
-unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows, int64_t row_bytes,
-                             int64_t nvec, int64_t chunks, const int32_t* __restrict__ si,
-                             int64_t topk, const void* __restrict__ pp,
-                             const int32_t* __restrict__ out_index, const int32_t* __restrict__ ptr,
-                             int64_t T, uint8_t* __restrict__ out) {
-    using V = Vec<TDT>;
-    pdl_enter();
-    const int lane = threadIdx.x & 31;
-    const int64_t items = T * chunks;
-    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < items;
-         item += nw) {
-        const int64_t t = item / chunks;
-        const int64_t v0 = (item - t * chunks) * (32 * kRedVQ) + lane;
-        int64_t L0, L1;
-        if (PADDED) {
-            L0 = ptr[t];
-            L1 = ptr[t + 1];
-        } else {
-            L0 = t * topk;
-            L1 = L0 + topk;
-        }
-        float acc[kRedVQ][V::N];
-#pragma unroll
-        for (int q = 0; q < kRedVQ; ++q)
-#pragma unroll
-            for (int k = 0; k < V::N; ++k) acc[q][k] = 0.0f;
-
-        for (int64_t g0 = L0; g0 < L1; g0 += 32) {
-            // this lane's slot of the group: row offset and weight
-            const int64_t e = g0 + lane;
-            bool keep = false;
-            int64_t roff = 0;
-            float w = 1.0f;
-            if (e < L1) {
-                int64_t r;
-                if (PADDED) {
-                    r = out_index[e];
-                    keep = true;
-                } else {
-                    const int32_t v = si[e];
-                    keep = v >= 0 && (int64_t)v < rows;
-                    r = v;
-                }
-                if (HAS_PROBS && keep) {
-                    w = ld_f32<PDT>(pp, PADDED ? r : e);
-                    keep = w != 0.0f;
-                }
-                roff = r * row_bytes;
-            }
-            uint32_t bal = __ballot_sync(0xffffffffu, keep);
-            while (bal) {
-                int src[kRedUnroll];
-                int cnt = 0;
-#pragma unroll
-                for (int u = 0; u < kRedUnroll; ++u) {
-                    src[u] = bal ? __ffs(bal) - 1 : 0;
-                    if (bal) {
-                        bal &= bal - 1u;
-                        ++cnt;
-                    }
-                }
-                uint4 x[kRedUnroll][kRedVQ];
-#pragma unroll
-                for (int u = 0; u < kRedUnroll; ++u) {
-                    const int64_t ro = __shfl_sync(0xffffffffu, roff, src[u]);
-                    if (u < cnt) {
-#pragma unroll
-                        for (int q = 0; q < kRedVQ; ++q) {
-                            const int64_t v = v0 + 32 * q;
-                            if (v < nvec) x[u][q] = ld_stream_v4(permuted + ro + 16 * v);
-                        }
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kRedUnroll; ++u) {
-                    const float wu = __shfl_sync(0xffffffffu, w, src[u]);
-                    if (u < cnt) {
-#pragma unroll
-                        for (int q = 0; q < kRedVQ; ++q) {
-                            const int64_t v = v0 + 32 * q;
-                            if (v < nvec) {
-                                float xs[V::N];
-                                V::unpack(x[u][q], xs);
-#pragma unroll
-                                for (int k = 0; k < V::N; ++k)
-                                    acc[q][k] = HAS_PROBS ? __fadd_rn(acc[q][k], __fmul_rn(xs[k], wu))
-                                                          : __fadd_rn(acc[q][k], xs[k]);
-                            }
-                        }
-                    }
-                }
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < kRedVQ; ++q) {
-            const int64_t v = v0 + 32 * q;
-            if (v < nvec) st_stream_v4(out + t * row_bytes + 16 * v, V::pack(acc[q]));
-        }
-    }
-}
-
-// Element-wise variant for rows that are not 16-byte vectors (odd H or
-// buffers not 16-byte aligned; element alignment is required). Same list,
-// same order, same arithmetic.
-template <int TDT, int PDT, bool HAS_PROBS, bool PADDED>
-__global__ void __launch_bounds__(256)
-unpermute_reduce_scalar_kernel(const uint8_t* __restrict__ permuted, int64_t rows, int64_t H,
-                               const int32_t* __restrict__ si, int64_t topk,
-                               const void* __restrict__ pp, const int32_t* __restrict__ out_index,
-                               const int32_t* __restrict__ ptr, int64_t T,
-                               uint8_t* __restrict__ out) {
-    __shared__ int64_t s_row[kListCap];
-    __shared__ float s_w[kListCap];
-    __shared__ int s_cnt;
-    constexpr int es = TDT == MR_DTYPE_F32 ? 4 : 2;
-    pdl_enter();
-    const int64_t row_bytes = H * es;
-    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
-        int64_t L0, L1;
-        if (PADDED) {
-            L0 = ptr[t];
-            L1 = ptr[t + 1];
-        } else {
-            L0 = t * topk;
-            L1 = L0 + topk;
-        }
-        for (int64_t h0 = 0; h0 < H; h0 += blockDim.x) {
-            const int64_t h = h0 + threadIdx.x;
-            float acc = 0.0f;
-            for (int64_t c0 = L0; c0 < L1; c0 += kListCap) {
-                const int64_t c1 = c0 + kListCap < L1 ? c0 + kListCap : L1;
-                if (threadIdx.x < 32) {
-                    const int cnt = build_list<HAS_PROBS, PADDED, PDT>(c0, c1, si, rows, row_bytes,
-                                                                       pp, out_index, s_row, s_w);
-                    if (threadIdx.x == 0) s_cnt = cnt;
-                }
-                __syncthreads();
-                const int cnt = s_cnt;
-                if (h < H) {
-                    for (int m = 0; m < cnt; ++m) {
-                        const uint8_t* rp = permuted + s_row[m] + h * es;
-                        float x;
-                        if constexpr (TDT == MR_DTYPE_F32) {
-                            x = __ldg(reinterpret_cast<const float*>(rp));
-                        } else {
-                            x = Elem<TDT>::to_f32(__ldg(reinterpret_cast<const unsigned short*>(rp)));
-                        }
-                        acc = HAS_PROBS ? __fadd_rn(acc, __fmul_rn(x, s_w[m])) : __fadd_rn(acc, x);
-                    }
-                }
-                __syncthreads();
-            }
-            if (h < H) {
-                uint8_t* op = out + t * row_bytes + h * es;
-                if constexpr (TDT == MR_DTYPE_F32) {
-                    *reinterpret_cast<float*>(op) = acc;
-                } else {
-                    *reinterpret_cast<uint16_t*>(op) = Elem<TDT>::from_f32(acc);
-                }
-            }
-        }
     }
 }
 
