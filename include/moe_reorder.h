@@ -11,6 +11,9 @@
  *                      功能说明与计算公式 (derived sizes, four branches),
  *                      参数说明 / 补充说明 (shapes, ranges), 约束说明,
  *                      返回值与错误码, Kernel 实现 (skip rules, fp32 math).
+ * and around them: the batching from a ScheduleContext, its full-tail option,
+ * the routing-map permute that produces the unpermute's input, and
+ * MoeUpdateExpert ("MoeUpdateExpert"), declared further down.
  *
  * Conventions shared by every entry point
  *  - Pointers named as device pointers must point to device memory of the
@@ -28,6 +31,12 @@
  *    CUDA runtime reports at launch return MR_ERR_CUDA.
  *  - Outputs must not alias inputs or each other.
  *  - Results are deterministic: identical inputs give identical bits.
+ *  - Execute calls can be captured into a CUDA graph (stream capture): they
+ *    only enqueue kernels, memsets and event records/waits on `stream` and
+ *    the auxiliary stream, which joins back. Make one call of each kind
+ *    outside any capture first (it creates the auxiliary stream and caches
+ *    device queries), and capture ffnwb_batching_noalloc only after its
+ *    first call on the device.
  */
 #ifndef MOE_REORDER_H
 #define MOE_REORDER_H
