@@ -7,18 +7,22 @@
 // Launch sequence on the caller's stream (PDL-chained):
 //   not padded, probs : maskedSelect = column bitmasks -> csort prefix ->
 //                       scatter (+ zero tail)
-//   always            : stable sort of sortedIndices (one pass of the
-//                       counting-sort engine up to 4096 keys, else 2-3 LSD
-//                       passes) -> outIndex, permuteTokenId; padded: the
-//                       per-token row ranges (CSR) are the one pass's key
-//                       starts, or built from the sorted keys
+//   always            : stable sort of sortedIndices -> outIndex,
+//                       permuteTokenId: one pass of the counting-sort engine
+//                       up to 4096 keys; padded up to 2^22 keys a pass on
+//                       the high bits and fine_sort_csr_kernel; else 2-3 LSD
+//                       passes. Padded, the per-token row ranges (CSR) are the
+//                       one pass's key starts, the fine sort's, or built from
+//                       the sorted keys
 //   padded, probs     : permuteProbs[i] = probs[sortedIndices[i], i // capacity],
 //                       written by the sort's first scatter
 //   not padded        : the sort runs on the library's auxiliary stream,
 //                       overlapping the gather-reduce (fork/join events)
-//   always            : gather-reduce, one warp per (token, hidden chunk),
-//                       fp32 accumulation in ascending slot / row order,
-//                       atomic-free, one RNE cast per output element.
+//   always            : gather-reduce (reduce.cuh), one warp per (token,
+//                       hidden chunk), fp32 accumulation in ascending slot /
+//                       row order, atomic-free, one RNE cast per output
+//                       element; launched in plain stream order when short
+//                       and the sort runs beside it.
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
