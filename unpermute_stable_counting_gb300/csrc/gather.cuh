@@ -15,7 +15,7 @@ namespace mr {
 // nvec - 1 lie inside [win, src + bytes); the last output vector is read as
 // words. The caller uses this only when the buffer base is 16-byte aligned,
 // so win never precedes the buffer.
-constexpr int kShiftVPT = 4;
+constexpr int kShiftVPT = 8;
 
 __device__ __forceinline__ uint4 shift_combine(const uint4& a, const uint4& b, int o) {
     if (o == 4) return make_uint4(a.y, a.z, a.w, b.x);
@@ -134,8 +134,11 @@ batching_gather_kernel(const uint8_t* __restrict__ token_data_arg, int64_t row_s
     const bool base16 = (reinterpret_cast<uintptr_t>(token_data) & 15u) == 0u;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    // the next row's source index is loaded while the current row copies
+    int64_t gnext = gw < (int64_t)U ? gather_idx[gw] : 0;
     for (int64_t i = gw; i < (int64_t)U; i += nw) {
-        const int64_t g = gather_idx[i];
+        const int64_t g = gnext;
+        gnext = i + nw < (int64_t)U ? gather_idx[i + nw] : 0;
         warp_copy_row<VPT>(token_data + g * row_stride, y + i * row_bytes, row_bytes, lane, base16);
         if (is_int8) {
             const uint8_t* sp = scales ? scales + g * scale_stride : token_data + g * row_stride + row_bytes;
