@@ -139,19 +139,45 @@ MUTANTS = [
 ]
 
 
-@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
-def test_pins_catch_mutant(name, old, new, tmp_path):
+PIN_FILES = ["test_oracle_pins.py", "test_oracle_context_pins.py", "test_oracle_permute_pins.py",
+             "test_oracle_update_expert_pins.py", "test_oracle_full_tail_pins.py"]
+
+
+def run_mutant(name, old, new, workdir):
+    """Build the oracle with one planted mistake and run every pin suite on it.
+    Returns (anchor found, pins failed, pytest tail)."""
     src = open(SRC).read()
-    assert src.count(old) >= 1, f"mutant {name}: anchor text not found"
-    mutant_src = tmp_path / "oracle_mutant.cpp"
-    mutant_src.write_text(src.replace(old, new))
-    lib = oracle.compile_library(str(mutant_src), str(tmp_path / "liboracle_mutant.so"))
+    if src.count(old) < 1:
+        return False, False, ""
+    mutant_src = os.path.join(workdir, f"{name}.cpp")
+    with open(mutant_src, "w") as f:
+        f.write(src.replace(old, new))
+    lib = oracle.compile_library(mutant_src, os.path.join(workdir, f"lib{name}.so"))
     env = dict(os.environ, USC_ORACLE_LIB=lib)
-    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
-                        os.path.join(HERE, "test_oracle_pins.py"),
-                        os.path.join(HERE, "test_oracle_context_pins.py"),
-                        os.path.join(HERE, "test_oracle_permute_pins.py"),
-                        os.path.join(HERE, "test_oracle_update_expert_pins.py"),
-                        os.path.join(HERE, "test_oracle_full_tail_pins.py")],
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider"]
+                       + [os.path.join(HERE, f) for f in PIN_FILES],
                        cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
-    assert r.returncode != 0, f"mutant {name} passed every pin:\n{r.stdout[-2000:]}"
+    return True, r.returncode != 0, r.stdout[-2000:]
+
+
+@pytest.fixture(scope="module")
+def mutant_results(tmp_path_factory):
+    """name -> result. In a plain run every mutant is built and checked at
+    once (independent compile + pytest processes); under pytest-xdist, whose
+    workers each run this fixture, every test runs its own mutant only."""
+    workdir = str(tmp_path_factory.mktemp("mutants"))
+    by_name = {m[0]: m for m in MUTANTS}
+    if os.environ.get("PYTEST_XDIST_WORKER"):
+        return lambda name: run_mutant(*by_name[name], workdir)
+    from concurrent.futures import ThreadPoolExecutor
+    with ThreadPoolExecutor(max_workers=max(2, min(8, os.cpu_count() or 2))) as ex:
+        futs = {name: ex.submit(run_mutant, *m, workdir) for name, m in by_name.items()}
+        done = {name: f.result() for name, f in futs.items()}
+    return lambda name: done[name]
+
+
+@pytest.mark.parametrize("name", [m[0] for m in MUTANTS])
+def test_pins_catch_mutant(name, mutant_results):
+    found, caught, tail = mutant_results(name)
+    assert found, f"mutant {name}: anchor text not found"
+    assert caught, f"mutant {name} passed every pin:\n{tail}"
