@@ -524,11 +524,14 @@ int oracle_permute(const void* tokens, const int8_t* routingMap, int64_t T, int6
 //  * balancedExpertIds[b, k] = eplbTable[e, 1 + c] with e = expertIds[b, k]
 //    and c = localRankId % count (balanceMode 0, by rank) or b % count
 //    (balanceMode 1, by token); -1 when e is outside [0, moeExpertNum) or
-//    count is outside [1, F - 1].
+//    count is outside [1, F - 1]. The page names the two modes but gives no
+//    rule for which instance: parity unpinned beyond the result being one of
+//    the expert's instances (and the same for every token of a rank in
+//    mode 0, cycling over the tokens in mode 1).
 //  * With scales and thresholds: balancedActiveMask[b, k] = the token is
-//    active (activeMask[b], all active if not given) and
-//    f32(scale[b, k]) >= threshold[k] (pruned when below). Without them the
-//    mask is not written.
+//    active (activeMask[b], all active if not given) and not
+//    f32(scale[b, k]) < threshold[k] (pruned when below; equal and NaN are
+//    kept). Without them the mask is not written.
 //  * expertIds and the output are int32 (idBytes 4) or int64 (idBytes 8).
 // ---------------------------------------------------------------------------
 int oracle_update_expert(const void* expertIds, int32_t idBytes, const int32_t* table,
