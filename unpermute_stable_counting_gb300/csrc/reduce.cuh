@@ -26,7 +26,8 @@ __device__ __forceinline__ float ld_f32(const void* base, int64_t i) {
 // ---------------------------------------------------------------------------
 constexpr int kListCap = 512;   // list entries per pass of the element-wise kernel
 constexpr int kRedUnroll = 4;   // rows in flight per warp step
-constexpr int kRedVQ = 2;       // 16-byte vectors per lane per work item
+constexpr int kRedVQ = 2;       // 16-byte vectors per lane per hidden chunk
+constexpr int kRedRun = 2;      // hidden chunks per work unit (one slot-list read)
 
 template <bool HAS_PROBS, bool PADDED, int PDT>
 __device__ __forceinline__ int build_list(int64_t c0, int64_t c1, const int32_t* __restrict__ si,
@@ -122,12 +123,16 @@ unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows,
     using V = Vec<TDT>;
     pdl_enter();
     const int lane = threadIdx.x & 31;
-    const int64_t items = T * chunks;
+    // A work unit is a run of kRedRun consecutive hidden chunks of one token:
+    // the token's slot list is read once for the run.
+    const int64_t runs = (chunks + kRedRun - 1) / kRedRun;
+    const int64_t units = T * runs;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t item = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; item < items;
-         item += nw) {
-        const int64_t t = item / chunks;
-        const int64_t v0 = (item - t * chunks) * (32 * kRedVQ) + lane;
+    for (int64_t unit = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; unit < units;
+         unit += nw) {
+        const int64_t t = unit / runs;
+        const int64_t c0 = (unit - t * runs) * kRedRun;
+        const int64_t c1 = c0 + kRedRun < chunks ? c0 + kRedRun : chunks;
         int64_t L0, L1;
         if (PADDED) {
             L0 = ptr[t];
@@ -136,6 +141,31 @@ unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows,
             L0 = t * topk;
             L1 = L0 + topk;
         }
+        // this lane's entry of the list's first 32 (kept across the run)
+        bool keep0 = false;
+        int64_t roff0 = 0;
+        float w0 = 1.0f;
+        {
+            const int64_t e = L0 + lane;
+            if (e < L1) {
+                int64_t r;
+                if (PADDED) {
+                    r = out_index[e];
+                    keep0 = true;
+                } else {
+                    const int32_t v = si[e];
+                    keep0 = v >= 0 && (int64_t)v < rows;
+                    r = v;
+                }
+                if (HAS_PROBS && keep0) {
+                    w0 = ld_f32<PDT>(pp, PADDED ? r : e);
+                    keep0 = w0 != 0.0f;
+                }
+                roff0 = r * row_bytes;
+            }
+        }
+        for (int64_t c = c0; c < c1; ++c) {
+        const int64_t v0 = c * (32 * kRedVQ) + lane;
         float acc[kRedVQ][V::N];
 #pragma unroll
         for (int q = 0; q < kRedVQ; ++q)
@@ -145,24 +175,29 @@ unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows,
         for (int64_t g0 = L0; g0 < L1; g0 += 32) {
             // this lane's slot of the group: row offset and weight
             const int64_t e = g0 + lane;
-            bool keep = false;
-            int64_t roff = 0;
-            float w = 1.0f;
-            if (e < L1) {
-                int64_t r;
-                if (PADDED) {
-                    r = out_index[e];
-                    keep = true;
-                } else {
-                    const int32_t v = si[e];
-                    keep = v >= 0 && (int64_t)v < rows;
-                    r = v;
+            bool keep = keep0;
+            int64_t roff = roff0;
+            float w = w0;
+            if (g0 != L0) {
+                keep = false;
+                roff = 0;
+                w = 1.0f;
+                if (e < L1) {
+                    int64_t r;
+                    if (PADDED) {
+                        r = out_index[e];
+                        keep = true;
+                    } else {
+                        const int32_t v = si[e];
+                        keep = v >= 0 && (int64_t)v < rows;
+                        r = v;
+                    }
+                    if (HAS_PROBS && keep) {
+                        w = ld_f32<PDT>(pp, PADDED ? r : e);
+                        keep = w != 0.0f;
+                    }
+                    roff = r * row_bytes;
                 }
-                if (HAS_PROBS && keep) {
-                    w = ld_f32<PDT>(pp, PADDED ? r : e);
-                    keep = w != 0.0f;
-                }
-                roff = r * row_bytes;
             }
             uint32_t bal = __ballot_sync(0xffffffffu, keep);
             while (bal) {
@@ -212,6 +247,7 @@ unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows,
         for (int q = 0; q < kRedVQ; ++q) {
             const int64_t v = v0 + 32 * q;
             if (v < nvec) st_stream_v4(out + t * row_bytes + 16 * v, V::pack(acc[q]));
+        }
         }
     }
 }
