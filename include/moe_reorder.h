@@ -93,9 +93,10 @@ typedef int32_t mr_status;
  *                BS > 0, topK+1 in (0,64], H > 0. Y = A*BS*(topK+1) must be
  *                below 2^31.
  *   tokenDtype   MR_DTYPE_F16, MR_DTYPE_BF16 or MR_DTYPE_INT8.
- *   needSchedule 0 (batching only). 1 (scan the ScheduleContext first) is a
- *                valid value on the page that this library does not
- *                implement: MR_ERR_UNSUPPORTED.
+ *   needSchedule 0 (batching only). 1 (scan the ScheduleContext first) needs
+ *                the context's flags, which flat arrays do not have:
+ *                MR_ERR_UNSUPPORTED here; ffnwb_batching_context
+ *                implements it.
  *   layerNum     in [0, expertNum]; expertNum must be a multiple of
  *                max(layerNum, 1).
  *   Returns MR_OK, MR_ERR_PARAM_NULLPTR (maxOutShape or workspaceSize NULL),
@@ -112,7 +113,8 @@ mr_status ffnwb_batching_get_workspace_size(int64_t expertNum, const int64_t* ma
  *     y[i] = token_data[gather_idx[i]]           (+ dynamic scale, INT8)
  *     group_list[e] = [expert_id_e, expert_token_num_e]
  *     actual_token_num = sum_e expert_token_num_e
- *   The page's ScheduleContext is replaced by flat arrays of the Y slots.
+ *   The page's ScheduleContext is replaced by flat arrays of the Y slots
+ *   (ffnwb_batching_context takes the context itself).
  *
  *   Inputs (device pointers unless noted; Y = A*BS*(topK+1) slots):
  *   expertIds       int32 [Y]: local expert id of each slot. A slot is masked
