@@ -1,0 +1,130 @@
+"""Seeded random sweep over shapes, dtypes and modes of every operation, each
+case compared with the oracle (bit for bit; the unpermute also within the
+stated tolerance). The parameters of case i are drawn from a generator seeded
+with i, so a failing case is reproducible from its id alone."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as w
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import unpermute_stable_counting_gb300 as usc  # noqa: E402
+
+from _gpu_util import (assert_batching_equal, assert_unpermute_equal, batching_numpy, dev,  # noqa: E402
+                       float_tensor, run_batching, run_unpermute, to_dev, unpermute_numpy)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+@pytest.mark.parametrize("case", range(48))
+def test_batching_random(case):
+    r = np.random.default_rng(1000 + case)
+    dt = int(r.integers(0, 3))
+    L = int(r.choice([1, 1, 2, 4]))
+    El = int(r.choice([1, 3, 8, 33, 256, 1000]))
+    A, BS, K1 = int(r.integers(1, 9)), int(r.integers(1, 40)), int(r.integers(1, 12))
+    H = int(r.choice([1, 8, 24, 136, 200, 1000] if dt != 2 else [4, 16, 100, 128, 512]))
+    inp = w.make_batching(A=A, BS=BS, K1=K1, E=El * L, H=H, dtype=dt, layerNum=L,
+                          layer_id=int(r.integers(0, L)), ids=str(r.choice(["uniform", "zipf", "mod"])),
+                          mask=float(r.choice([0.0, 0.1, 0.5, 1.0])), session=3, micro=5,
+                          token_ids=bool(r.integers(0, 2)), seed=case,
+                          separate_scales=bool(dt == 2 and r.integers(0, 2)))
+    ref = oracle.batching(inp)
+    got = batching_numpy(run_batching(inp, token_ids=inp.get("token_in") is not None), inp)
+    assert_batching_equal(got, ref)
+
+
+@pytest.mark.parametrize("case", range(48))
+def test_unpermute_random(case):
+    r = np.random.default_rng(2000 + case)
+    dt = int(r.choice([0, 1, 3]))
+    with_probs = bool(r.integers(0, 4) > 0)
+    pdt = (dt if r.integers(0, 2) else 3) if with_probs else None
+    H = int(r.choice([1, 7, 8, 64, 136, 520]))
+    if r.integers(0, 2):
+        Eu = int(r.choice([4, 16, 64]))
+        k = int(r.choice([1, 2, 4]))
+        T = Eu * int(r.integers(1, 40))
+        inp = w.make_unpermute_padded(T=T, Eu=Eu, k=k, H=H, dtype=dt, probs_dtype=pdt,
+                                      mult=int(r.choice([1, 3, 5, 7])), seed=case)
+        si = inp["sortedIndices"].copy()
+        bad = r.random(si.size) < float(r.choice([0.0, 0.2]))
+        si[bad] = r.choice([-1, T, T + 100], size=int(bad.sum())).astype(np.int32)
+        inp = dict(inp, sortedIndices=si)
+    else:
+        T = int(r.integers(1, 400))
+        k = int(r.choice([1, 2, 5, 8, 13]))
+        Eu = int(r.integers(k, 3 * k + 5))
+        inp = w.make_unpermute_topk(T=T, k=k, Eu=Eu, H=H, dtype=dt, probs_dtype=pdt,
+                                    choices=tuple(sorted({1, k // 2 + 1, k})), seed=case)
+    ref = oracle.unpermute(inp)
+    got = unpermute_numpy(run_unpermute(inp), inp)
+    assert_unpermute_equal(got, ref, inp)
+
+
+@pytest.mark.parametrize("case", range(32))
+def test_permute_random(case):
+    r = np.random.default_rng(3000 + case)
+    dt = int(r.choice([0, 1, 3]))
+    T, Eu = int(r.integers(1, 300)), int(r.choice([1, 5, 32, 40, 300]))
+    H = int(r.choice([1, 3, 8, 72, 256]))
+    m = (r.random((T, Eu)) < float(r.choice([0.0, 0.05, 0.3, 1.0]))).astype(np.int8)
+    x = w.normal_rows(T, H, dt, seed=case)
+    if r.integers(0, 2):
+        kw = dict(padded=1, capacity=int(r.integers(1, T + 3)))
+        api = dict(padded_mode=True, capacity=kw["capacity"])
+    else:
+        kw = dict(topK=int(r.integers(1, 12)))
+        api = dict(topk=kw["topK"])
+    ref = oracle.permute(x, m, tokenDtype=dt, **kw)
+    out = usc.moe_permute(float_tensor(x, dt), to_dev(m), **api)
+    torch.cuda.synchronize()
+    assert np.array_equal(out["sortedIndices"].cpu().numpy(), ref["sortedIndices"])
+    rows = ref["rows"]
+    assert int(out["permutedRows"][0]) == rows
+    t = out["permutedTokens"]
+    got = t.cpu().numpy() if dt == 3 else t.view(torch.int16).cpu().numpy().view(np.uint16)
+    if kw.get("padded"):
+        assert np.array_equal(got.view(np.uint8), ref["permuted"].view(np.uint8))  # padding rows are zero
+    else:
+        assert np.array_equal(got[:rows].view(np.uint8), ref["permuted"][:rows].view(np.uint8))
+
+
+@pytest.mark.parametrize("case", range(32))
+def test_update_expert_random(case):
+    r = np.random.default_rng(4000 + case)
+    ws = int(r.integers(2, 64))
+    ppr = int(r.integers(1, 1024 // ws + 1))
+    E = int(r.integers(1, min(1024, ws * ppr) + 1))
+    K = int(r.integers(1, min(16, E) + 1))
+    BS = int(r.integers(1, 513))
+    sdt = int(r.choice([0, 1, 3]))
+    idt = np.int64 if r.integers(0, 2) else np.int32
+    inp = w.make_update_expert(BS=BS, K=K, moe_expert_num=E, world_size=ws, place_per_rank=ppr,
+                               scales_dtype=sdt, id_dtype=idt, active_frac=float(r.random()), seed=case)
+    ids = inp["expert_ids"].copy()
+    ids[r.random(ids.shape) < 0.05] = -1
+    mode, rank = int(r.integers(0, 2)), int(r.integers(0, ws))
+    prune = bool(r.integers(0, 3) > 0)
+    ref = oracle.update_expert(ids, inp["table"], local_rank=rank, balance_mode=mode,
+                               scales=inp["scales"] if prune else None, scales_dtype=sdt,
+                               threshold=inp["threshold"] if prune else None,
+                               active=inp["active"] if prune else None)
+    out = usc.moe_update_expert(to_dev(ids), to_dev(inp["table"]), local_rank=rank, world_size=ws,
+                                balance_mode=mode, scales=float_tensor(inp["scales"], sdt) if prune else None,
+                                threshold=to_dev(inp["threshold"]) if prune else None,
+                                active=to_dev(inp["active"]) if prune else None)
+    torch.cuda.synchronize()
+    assert np.array_equal(out["balancedExpertIds"].cpu().numpy(), ref["balancedExpertIds"])
+    if prune:
+        assert np.array_equal(out["balancedActiveMask"].cpu().numpy(), ref["balancedActiveMask"])
