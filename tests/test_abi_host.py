@@ -354,3 +354,27 @@ def test_context_ex_flags(L, flags, kw, expect):
                                      a["to"], a["eo"], a["dyn"], a["atn"], a["status"], flags, a["ws"],
                                      a["wsz"], a["stream"])
     assert st == expect
+
+
+def _no_gpu():
+    try:
+        import torch
+        return not torch.cuda.is_available()
+    except Exception:
+        return True
+
+
+@pytest.mark.skipif(not _no_gpu(), reason="forces launch failures, which need a machine without a GPU")
+def test_launch_failures_return_cuda_error(L):
+    """Valid arguments on a machine without a GPU: the checks pass, the first
+    CUDA call fails, and the call returns MR_ERR_CUDA (no kernel runs, so the
+    placeholder pointers are never touched)."""
+    CUDA = 561001
+    assert _batching_call(L) == CUDA
+    assert _context_call(L) == CUDA
+    assert _permute_call(L) == CUDA
+    assert _update_call(L) == CUDA
+    assert _update_call(L, sc=FAKE, thr=FAKE, mask=FAKE) == CUDA
+    # the not-padded unpermute first needs its auxiliary stream
+    assert _unpermute_call(L) == CUDA
+    assert _unpermute_call(L, padded=1) == CUDA
