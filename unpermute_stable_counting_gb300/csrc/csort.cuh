@@ -16,6 +16,8 @@
 //                  (bucket_start) plus an optional compacted
 //                  [key, count] list of the non-empty buckets below a limit.
 //   consumers:     elementwise kernels of each operation call csort_dest().
+//   single tile:   an input of at most one tile sorts in one block
+//                  (csort_single_tile_kernel), scatter included.
 //
 // The stable in-tile rank: each of the kSortWarps warps owns kSortChunks
 // consecutive 32-item chunks of the tile and walks them in order. Within a
@@ -273,6 +275,117 @@ inline cudaError_t csort_run(KeyFn kf, int64_t N, int B, const CsortBufs& b, Gro
                                b.ticket);
     if (e != cudaSuccess) return e;
     return csort_prefix(b.tile_off, tiles, B, b.totals, b.bucket_start, b.ticket, gl, st);
+}
+
+// The whole sort of an input of one tile (at most kSortTile items) in one
+// block: the stable in-tile ranks as in csort_rank_kernel, the tile's
+// histogram scanned into key starts in shared memory (the key starts and the
+// optional compacted group list written out), then the consumer's scatter
+// step for every item, at start[key] + rank. One launch instead of rank,
+// prefix and scatter; no block waits on another.
+template <class KeyFn, class Consumer>
+static __global__ void __launch_bounds__(kSortThreads)
+csort_single_tile_kernel(KeyFn kf, int64_t Y, int B, uint32_t* __restrict__ bucket_start,
+                         GroupListOut gl, Consumer sc) {
+    extern __shared__ __align__(16) uint16_t tab[];  // [kSortWarps][B] u16, then [B + 1] u32
+    __shared__ uint32_t warp_sums[32];
+    pdl_enter();
+    uint32_t* bs = reinterpret_cast<uint32_t*>(tab + (kSortWarps * B + 7) / 8 * 8);  // 16-byte aligned
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int tab_words = (kSortWarps * B + 1) / 2;
+    uint32_t* tab32 = reinterpret_cast<uint32_t*>(tab);
+    for (int i = threadIdx.x; i < tab_words; i += kSortThreads) tab32[i] = 0u;
+    const int64_t base = (int64_t)warp * (32 * kSortChunks);
+    int key[kSortChunks];
+#pragma unroll
+    for (int c = 0; c < kSortChunks; ++c) {
+        const int64_t i = base + c * 32 + lane;
+        key[c] = i < Y ? kf(i) : -1;
+    }
+    __syncthreads();
+    uint16_t* mytab = tab + warp * B;
+    uint32_t rnk[kSortChunks];
+    const uint32_t lt = lanemask_lt();
+#pragma unroll
+    for (int c = 0; c < kSortChunks; ++c) {
+        const int k = key[c];
+        const uint32_t peers = __match_any_sync(0xffffffffu, k);
+        const uint32_t below = __popc(peers & lt);
+        uint32_t before = 0u;
+        if (k >= 0) before = mytab[k];
+        __syncwarp();
+        if (k >= 0 && below == 0u) mytab[k] = (uint16_t)(before + __popc(peers));
+        __syncwarp();
+        rnk[c] = before + below;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int c = 0; c < kSortChunks; ++c) {
+        const int k = key[c];
+        if (k >= 0)
+            for (int w = 0; w < warp; ++w) rnk[c] += tab[w * B + k];
+    }
+    for (int k = threadIdx.x; k < B; k += kSortThreads) {
+        uint32_t s = 0u;
+#pragma unroll
+        for (int w = 0; w < kSortWarps; ++w) s += tab[w * B + k];
+        bs[k] = s;
+    }
+    __syncthreads();
+    // key starts: each thread scans a run of consecutive keys
+    const int per_t = (B + kSortThreads - 1) / kSortThreads;
+    const int c0 = threadIdx.x * per_t < B ? threadIdx.x * per_t : B;
+    const int c1 = c0 + per_t < B ? c0 + per_t : B;
+    uint32_t s = 0u, ng = 0u;
+    for (int k = c0; k < c1; ++k) {
+        s += bs[k];
+        if (k < gl.limit && bs[k] != 0u) ++ng;
+    }
+    uint32_t total = 0u, groups = 0u;
+    const uint32_t excl = block_exclusive_scan(s, warp_sums, &total);
+    const uint32_t gexcl = block_exclusive_scan(ng, warp_sums, &groups);
+    uint32_t run = excl, r = gexcl;
+    for (int k = c0; k < c1; ++k) {
+        const uint32_t v = bs[k];
+        bs[k] = run;
+        bucket_start[k] = run;
+        if (gl.rows && k < gl.limit && v != 0u) {
+            gl.rows[2 * (int64_t)r] = k;
+            gl.rows[2 * (int64_t)r + 1] = v;
+            ++r;
+        }
+        run += v;
+    }
+    if (threadIdx.x == 0) {
+        bs[B] = total;
+        bucket_start[B] = total;
+    }
+    if (gl.rows)
+        for (int64_t q = (int64_t)groups + threadIdx.x; q < gl.limit; q += kSortThreads) {
+            gl.rows[2 * q] = 0;
+            gl.rows[2 * q + 1] = 0;
+        }
+    __syncthreads();
+    if (gl.count_out && threadIdx.x == 0) *gl.count_out = (int64_t)bs[gl.limit];
+#pragma unroll
+    for (int c = 0; c < kSortChunks; ++c) {
+        const int k = key[c];
+        if (k >= 0) sc(base + c * 32 + lane, k, bs[k] + rnk[c], bs[k]);
+    }
+}
+
+// Launch of csort_single_tile_kernel for N <= kSortTile items.
+template <class KeyFn, class Consumer>
+inline cudaError_t csort_single_tile(KeyFn kf, int64_t N, int B, const CsortBufs& b, GroupListOut gl,
+                                     const Consumer& cons, cudaStream_t st) {
+    const size_t smem = align_up((uint64_t)kSortWarps * B * 2u, 16) + align_up((uint64_t)(B + 1) * 4u, 16);
+    auto kernel = csort_single_tile_kernel<KeyFn, Consumer>;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(kernel, dim3(1), dim3(kSortThreads), smem, st, kf, N, B, b.bucket_start, gl, cons);
 }
 
 }  // namespace mr

@@ -546,10 +546,15 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
             RadixScatter sc{kf, iin, keys[pass & 1], last ? nullptr : idx[pass & 1],
                             last ? outIndex : nullptr, last ? permuteTokenId : nullptr,
                             p.topk > 0 ? p.topk : (int64_t)1, ppr};
-            cudaError_t e = csort_run(kf, p.n, B, cs, none, ss);
-            if (e != cudaSuccess) return e;
-            e = launch_pdl(radix_scatter_kernel, dim3(elementwise_grid(p.n)), dim3(256), 0, ss, kf, p.n, B,
-                           cs, sc);
+            cudaError_t e;
+            if (p.n <= kSortTile) {
+                e = csort_single_tile(kf, p.n, B, cs, none, sc, ss);  // one block
+            } else {
+                e = csort_run(kf, p.n, B, cs, none, ss);
+                if (e != cudaSuccess) return e;
+                e = launch_pdl(radix_scatter_kernel, dim3(elementwise_grid(p.n)), dim3(256), 0, ss, kf,
+                               p.n, B, cs, sc);
+            }
             if (e != cudaSuccess) return e;
             kin = keys[pass & 1];
             iin = idx[pass & 1];
