@@ -56,7 +56,7 @@ def parse_args(argv=None):
                     help="attention workers (A) of the oracle's bounded sample (full workload: 256)")
     ap.add_argument("--small", action="store_true", help="a small case of the same workload (profiling)")
     ap.add_argument("--workload", choices=["roundtrip", "tiny", "topk", "int8", "padded", "context",
-                                           "batching", "permute", "permute_padded", "update_expert"],
+                                           "batching", "permute", "permute_padded", "update_expert", "decode_unpermute"],
                     default="roundtrip",
                     help="roundtrip (the bench line) or one of the other workloads, timed per call "
                          "with an L2 flush before each")
@@ -673,6 +673,8 @@ def run_workload(args):
     else:
         if name == "topk":
             u = w.make_unpermute_topk(**w.UNPERMUTE_TOPK)
+        elif name == "decode_unpermute":
+            u = w.make_unpermute_topk(**w.UNPERMUTE_DECODE)
         else:
             u = w.make_unpermute_padded(**w.UNPERMUTE_PADDED)
         T, H, n, dt, pdt, Eu = u["T"], u["H"], u["n"], u["tokenDtype"], u["probsDtype"], u["Eu"]

@@ -254,6 +254,8 @@ BATCHING_INT8_DECODE = dict(A=64, BS=32, K1=9, E=256, H=7168, dtype=DT_INT8, lay
                             micro=64, token_ids=True, seed=2)
 UNPERMUTE_TOPK = dict(T=4096, k=8, Eu=64, H=4096, dtype=DT_BF16, probs_dtype=DT_BF16, seed=1)
 UNPERMUTE_PADDED = dict(T=16384, Eu=128, k=4, H=4096, dtype=DT_F16, probs_dtype=DT_F32, seed=3)
+# a decode-sized step: 64 tokens, each routed to 6-8 of 64 experts, H = 7168 bf16
+UNPERMUTE_DECODE = dict(T=64, k=8, Eu=64, H=7168, dtype=DT_BF16, probs_dtype=DT_BF16, seed=7)
 ROUNDTRIP_BATCHING = dict(A=256, BS=64, K1=9, E=1024, H=7168, dtype=DT_BF16, layerNum=4,
                           layer_id=2, ids="zipf", zipf_s=1.2, mask=0.05, session=256, micro=64,
                           token_ids=True, seed=4)
