@@ -1,7 +1,7 @@
 """PyTorch-facing binding of the C ABI (include/moe_reorder.h).
 
 Argument marshalling only: shapes, dtypes and device pointers of torch CUDA
-tensors go to the library; every step of both operations runs in the
+tensors go to the library; every step of every operation runs in the
 library's CUDA kernels. PyTorch supplies device memory (outputs and the
 workspace, when the caller does not pass them) and the current stream.
 """
@@ -17,7 +17,6 @@ DT_F16, DT_BF16, DT_INT8, DT_F32 = 0, 1, 2, 3
 _TORCH_TO_DT = {torch.float16: DT_F16, torch.bfloat16: DT_BF16, torch.float32: DT_F32}
 _DT_TO_TORCH = {DT_F16: torch.float16, DT_BF16: torch.bfloat16, DT_INT8: torch.int8,
                 DT_F32: torch.float32}
-_ELEM = {DT_F16: 2, DT_BF16: 2, DT_INT8: 1, DT_F32: 4}
 
 MR_OK = 0
 MR_BATCHING_FULL_TAIL = 1
