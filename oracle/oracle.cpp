@@ -1,7 +1,9 @@
 // Parity oracle for the MoE expert-grouped token reorder.
 //
 // TEST INFRASTRUCTURE ONLY. This file is a plain, slow, single-threaded CPU
-// restatement of what the two operations compute. Only the test suite, the
+// restatement of what the operations compute: the FFN-worker batching (from
+// flat arrays or a ScheduleContext, optionally over the whole tail), the
+// routing-map permute and unpermute, and MoeUpdateExpert. Only the test suite, the
 // smoke check and the benchmark's CPU-baseline leg may load it; the product
 // path (the CUDA library and its Python binding) never does. It shares no code,
 // header, table or helper with the CUDA path.
