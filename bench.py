@@ -112,17 +112,25 @@ def algorithmic_bytes(spec, U, V):
                 gather_kernel=gather, reduce_kernel=reduce_, tokens=T, slots=Y)
 
 
-def sort_passes(key_range):
+def sort_launches(n, key_range):
+    """Kernels of the unpermute's index sort over n entries with key_range
+    distinct keys, as the library plans it: one counting-sort pass (one
+    block-local kernel up to 2048 entries, else rank, prefix and scatter) up to
+    4096 keys; up to 2^22 keys that pass on the high bits plus the per-bucket
+    fine sort; beyond, LSD passes of at most 12 bits (not padded)."""
+    one_pass = 1 if n <= 2048 else 3
     if key_range <= 4096:
-        return 1
+        return one_pass
+    if key_range <= 1 << 22:
+        return one_pass + 1
     bits = int(np.ceil(np.log2(key_range)))
-    return (bits + 11) // 12
+    return 3 * ((bits + 11) // 12)
 
 
 def launches_per_step(spec):
     Y = spec["A"] * spec["BS"] * spec["K1"]
     batching = 4  # rank, prefix, scatter, gather
-    unpermute = 3 + 3 * sort_passes(Y + 1) + 1  # maskedSelect (3), sort passes, reduce
+    unpermute = 3 + sort_launches(Y, Y + 1) + 1  # maskedSelect (3), index sort, reduce
     return batching + unpermute
 
 

@@ -41,11 +41,15 @@ def test_roundtrip_workload_bytes_are_about_six_gigabytes():
 def test_launch_count():
     spec = bench.workload_spec()
     # batching: rank, prefix, scatter, gather; unpermute: maskedSelect (3),
-    # two sort passes of 3 launches (147457 keys -> 18 bits), reduce
-    assert bench.sort_passes(147457) == 2
-    assert bench.sort_passes(4096) == 1
-    assert bench.sort_passes(4097) == 1 + (13 > 12)
-    assert bench.launches_per_step(spec) == 4 + 3 + 6 + 1
+    # the index sort (147457 keys: a coarse pass of 3 launches and the fine
+    # sort), reduce
+    assert bench.sort_launches(147456, 147457) == 4
+    assert bench.sort_launches(3000, 4096) == 3
+    assert bench.sort_launches(512, 4096) == 1
+    assert bench.sort_launches(4096, 4097) == 4
+    assert bench.sort_launches(1 << 22, (1 << 22) + 1) == 6       # 23 bits: two LSD passes
+    assert bench.sort_launches(1 << 24, (1 << 24) + 1) == 9       # 25 bits: three
+    assert bench.launches_per_step(spec) == 4 + 3 + 4 + 1
 
 
 def test_contributing_rows_counts_valid_nonzero_slots():

@@ -127,15 +127,22 @@ SORT_CASES = {
                                               choices=(2, 8), seed=15),
     "one_pass_padded": lambda: w.make_unpermute_padded(T=4032, Eu=64, k=2, H=16, dtype=0,
                                                        probs_dtype=3, mult=9, seed=16),
-    # LSD passes, two and three of them, ragged tile counts
-    "passes_not_padded": lambda: w.make_unpermute_topk(T=1000, k=6, Eu=32, H=16, dtype=1, probs_dtype=1,
-                                                       choices=(2, 6), seed=11),
-    "passes_padded": lambda: w.make_unpermute_padded(T=8192, Eu=64, k=2, H=16, dtype=0,
-                                                     probs_dtype=3, mult=9, seed=10),
-    "passes_wide_not_padded": lambda: w.make_unpermute_topk(T=20000, k=8, Eu=32, H=16, dtype=1,
-                                                            probs_dtype=1, choices=(3, 8), seed=13),
-    "passes_wide_padded": lambda: w.make_unpermute_padded(T=32768, Eu=64, k=2, H=16, dtype=0,
-                                                          probs_dtype=3, mult=7, seed=14),
+    # two levels (a coarse pass, then a block per coarse bucket), ragged tile counts
+    "two_level_not_padded": lambda: w.make_unpermute_topk(T=1000, k=6, Eu=32, H=16, dtype=1, probs_dtype=1,
+                                                          choices=(2, 6), seed=11),
+    "two_level_padded": lambda: w.make_unpermute_padded(T=8192, Eu=64, k=2, H=16, dtype=0,
+                                                        probs_dtype=3, mult=9, seed=10),
+    "two_level_wide_not_padded": lambda: w.make_unpermute_topk(T=20000, k=8, Eu=32, H=16, dtype=1,
+                                                               probs_dtype=1, choices=(3, 8), seed=13),
+    "two_level_wide_padded": lambda: w.make_unpermute_padded(T=32768, Eu=64, k=2, H=16, dtype=0,
+                                                             probs_dtype=3, mult=7, seed=14),
+    # not padded, the first key count past one pass: 4096 rows, 3-bit fine keys
+    "two_level_not_padded_4097_keys": lambda: w.make_unpermute_topk(T=1024, k=4, Eu=8, H=8, dtype=1,
+                                                                    probs_dtype=1, choices=(1, 4), seed=21),
+    # not padded at the two-level limit (2^22 keys: 4097 coarse buckets, 10-bit
+    # fine keys) and one row past it (LSD passes)
+    "two_level_not_padded_max": lambda: permutation_case((1 << 22) - 1, seed=22),
+    "passes_not_padded_past_max": lambda: permutation_case(1 << 22, seed=23),
     # padded keys beyond 2^22: LSD passes and the CSR kernel
     "passes_padded_4m": lambda: w.make_unpermute_padded(T=1 << 22, Eu=16, k=1, H=4, dtype=0,
                                                         probs_dtype=3, mult=5, seed=19),
@@ -145,12 +152,41 @@ SORT_CASES = {
 }
 
 
+def permutation_case(rows, seed, invalid=0.1):
+    """Not padded, topK = 1, no probs: sortedIndices is a random permutation
+    of the rows with a fraction replaced by invalid indices (-1 and rows)."""
+    rng = np.random.default_rng(seed)
+    si = rng.permutation(rows).astype(np.int32)
+    bad = rng.random(rows) < invalid
+    si[bad] = np.where(rng.random(int(bad.sum())) < 0.5, -1, rows).astype(np.int32)
+    return dict(permuted=w.normal_rows(rows, 4, 0, seed), sortedIndices=si, routingMap=None, probs=None,
+                permutedRows=rows, H=4, tokenDtype=0, n=rows, probsDtype=0, T=rows, Eu=0, padded=0)
+
+
 @pytest.mark.parametrize("case", list(SORT_CASES))
 def test_index_sort_paths(case):
-    """The index sort's forms: one counting-sort pass over every key; padded,
-    a coarse pass on the high bits and a per-bucket fine sort that writes the
-    row pointers; and two or three LSD passes (keys beyond 2^24 take three)."""
+    """The index sort's forms: one counting-sort pass over every key; up to
+    2^22 keys a coarse pass on the high bits and a per-bucket fine sort (padded,
+    it also writes the row pointers; not padded, the invalid entries are
+    placed by the coarse pass); and two or three LSD passes beyond that (keys
+    beyond 2^24 take three)."""
     check(SORT_CASES[case]())
+
+
+@pytest.mark.parametrize("T,k", [(2048, 4), (16384, 9)])
+def test_not_padded_invalid_rows_and_duplicates(T, k):
+    """Two-level not-padded sort with 40% invalid slots (all in the coarse
+    bucket that the coarse pass places) and one row index repeated in 10% of
+    the slots (one fine key with thousands of entries, many 256-entry chunks
+    in one block)."""
+    inp = w.make_unpermute_topk(T=T, k=k, Eu=2 * k, H=24, dtype=1, probs_dtype=1, choices=(k,), seed=T + k)
+    rng = np.random.default_rng(T)
+    si = inp["sortedIndices"].copy()
+    bad = rng.random(si.size) < 0.4
+    si[bad] = np.where(rng.random(int(bad.sum())) < 0.5, -1, T * k + 3).astype(np.int32)
+    dup = rng.random(si.size) < 0.1
+    si[dup & ~bad] = 77
+    check(dict(inp, sortedIndices=si))
 
 
 @pytest.mark.parametrize("padded", [0, 1])

@@ -9,8 +9,8 @@
 //                       scatter (+ zero tail)
 //   always            : stable sort of sortedIndices -> outIndex,
 //                       permuteTokenId: one pass of the counting-sort engine
-//                       up to 4096 keys; padded up to 2^22 keys a pass on
-//                       the high bits and fine_sort_csr_kernel; else 2-3 LSD
+//                       up to 4096 keys; up to 2^22 keys a coarse pass on
+//                       the high bits and fine_sort_kernel; else 2-3 LSD
 //                       passes. Padded, the per-token row ranges (CSR) are the
 //                       one pass's key starts, the fine sort's, or built from
 //                       the sorted keys
@@ -72,9 +72,13 @@ mask_scatter_kernel(const int8_t* __restrict__ map, const uint32_t* __restrict__
 }
 
 // ---------------------------------------------------------------------------
-// Stable sort of sortedIndices (LSD passes of the counting-sort engine).
+// Stable sort of sortedIndices (LSD passes of the counting-sort engine, or a
+// coarse pass followed by one block per coarse bucket).
 // Full key: not padded (invalid first) v+1 for 0 <= v < rows, else 0;
 //           padded (invalid last)      v   for 0 <= v < T,    else T.
+// The coarse digit of the not-padded two-level sort keeps the invalid entries
+// alone in bucket 0 (1 + (key - 1) >> shift for the others), so that their
+// final places are known after the coarse pass.
 // ---------------------------------------------------------------------------
 struct RadixKey {
     const int32_t* si;        // pass 0 source
@@ -83,6 +87,7 @@ struct RadixKey {
     int padded;
     int shift;
     uint32_t mask;
+    int coarse_invalid_apart;  // not padded, two levels: digit as described above
     __device__ __forceinline__ uint32_t full(int64_t i) const {
         if (keys_in) return keys_in[i];
         const int32_t v = si[i];
@@ -90,9 +95,11 @@ struct RadixKey {
         if (padded) return ok ? (uint32_t)v : (uint32_t)limit;
         return ok ? (uint32_t)v + 1u : 0u;
     }
-    __device__ __forceinline__ int operator()(int64_t i) const {
-        return (int)((full(i) >> shift) & mask);
+    __device__ __forceinline__ int digit(uint32_t fk) const {
+        if (coarse_invalid_apart) return fk == 0u ? 0 : (int)(1u + ((fk - 1u) >> shift));
+        return (int)((fk >> shift) & mask);
     }
+    __device__ __forceinline__ int operator()(int64_t i) const { return digit(full(i)); }
 };
 
 // The padded probs lookup of the first pass (pp != nullptr): it reads the same
@@ -107,7 +114,10 @@ struct PaddedProbs {
 // The scatter step of one sort pass for item i at position d: the full key
 // and the item's original index move to d (every pass but the last); the last
 // pass writes outIndex and permuteTokenId instead. The first pass of a padded
-// sort with probs also writes permuteProbs[i].
+// sort with probs also writes permuteProbs[i]. In the coarse pass of the
+// not-padded two-level sort, an invalid entry (bucket 0, which starts at 0 and
+// keeps the original order) is already in its final place: it writes
+// outIndex and permuteTokenId at once (final_index, final_ptid).
 struct RadixScatter {
     RadixKey kf;
     const int32_t* idx_in;
@@ -117,6 +127,8 @@ struct RadixScatter {
     int32_t* ptid;
     int64_t topk;
     PaddedProbs pprobs;
+    int32_t* final_index;
+    int32_t* final_ptid;
     __device__ __forceinline__ void operator()(int64_t i, int, uint32_t d, uint32_t) const {
         if (pprobs.pp) {
             // permuteProbs[i] = probs[sortedIndices[i], i // capacity], 0 if invalid
@@ -129,6 +141,11 @@ struct RadixScatter {
         }
         const uint32_t fk = kf.full(i);
         const int32_t idx = idx_in ? idx_in[i] : (int32_t)i;
+        if (final_index && fk == 0u) {
+            final_index[d] = idx;
+            final_ptid[d] = (int32_t)(idx / topk);
+            return;
+        }
         keys_out[d] = fk;
         if (out_index) {
             out_index[d] = idx;
@@ -149,35 +166,43 @@ radix_scatter_kernel(RadixKey kf, int64_t n, int B, CsortBufs cs, RadixScatter s
     }
 }
 
-// Second level of the padded sort (one block per coarse bucket). The first
-// level is a counting-sort pass on key >> s, which leaves each coarse bucket
-// [cstart[c], cstart[c+1]) in original order. The block sorts its bucket
-// stably by the low s bits (F = 2^s fine keys): a histogram and its scan give
-// the fine starts -- which are the CSR row pointers ptr[c*F + f] -- and
-// 256-item chunks taken in order are ranked by key with warp matches, per-warp
-// counters and a running count per fine key.
+// Second level of the two-level sort (one block per coarse bucket). The first
+// level is a counting-sort pass on the coarse digit, which leaves each coarse
+// bucket [cstart[c], cstart[c+1]) in original order. The block sorts its
+// bucket stably by the low s bits of its key (F = 2^s fine keys): a histogram
+// and its scan give the fine starts, and 256-item chunks taken in order are
+// ranked by key with warp matches, per-warp counters and a running count per
+// fine key.
+//   padded:     digit key >> s, fine key = key & (F-1); the fine starts are
+//               the CSR row pointers ptr[c*F + f]; permuteTokenId = the value.
+//   not padded: bucket 0 holds the invalid entries, placed by the coarse
+//               pass; block b sorts bucket b+1 by (key - 1) & (F-1);
+//               permuteTokenId = original index / topK.
 constexpr int kFineThreads = 256;
 constexpr int kFineWarps = kFineThreads / 32;
 constexpr int kMaxFineBits = 10;
 
+template <bool PADDED>
 __global__ void __launch_bounds__(kFineThreads)
-fine_sort_csr_kernel(const uint32_t* __restrict__ keys, const int32_t* __restrict__ idx,
-                     const uint32_t* __restrict__ cstart, int shift, int64_t T,
-                     const int32_t* __restrict__ si, int32_t* __restrict__ out_index,
-                     int32_t* __restrict__ ptid, int32_t* __restrict__ ptr) {
+fine_sort_kernel(const uint32_t* __restrict__ keys, const int32_t* __restrict__ idx,
+                 const uint32_t* __restrict__ cstart, int shift, int64_t T, int64_t topk,
+                 const int32_t* __restrict__ si, int32_t* __restrict__ out_index,
+                 int32_t* __restrict__ ptid, int32_t* __restrict__ ptr) {
     extern __shared__ __align__(16) uint32_t fsm[];
     const int F = 1 << shift;
     uint32_t* hist = fsm;                     // [F] counts, then fine starts
     uint32_t* running = fsm + F;              // [F] items placed so far
     uint32_t* wcnt = fsm + 2 * F;             // [kFineWarps][F] this chunk's counts
     pdl_enter();
-    const int c = blockIdx.x;
+    const int c = PADDED ? (int)blockIdx.x : (int)blockIdx.x + 1;
     const uint32_t lo = cstart[c], hi = cstart[c + 1];
     const int warp = threadIdx.x >> 5;
     const uint32_t fmask = (uint32_t)F - 1u;
+    const uint32_t kofs = PADDED ? 0u : 1u;
     for (int i = threadIdx.x; i < (2 + kFineWarps) * F; i += kFineThreads) fsm[i] = 0u;
     __syncthreads();
-    for (uint32_t i = lo + threadIdx.x; i < hi; i += kFineThreads) atomicAdd(&hist[keys[i] & fmask], 1u);
+    for (uint32_t i = lo + threadIdx.x; i < hi; i += kFineThreads)
+        atomicAdd(&hist[(keys[i] - kofs) & fmask], 1u);
     __syncthreads();
     if (threadIdx.x == 0) {  // F <= 1024 counts: a serial scan is a few hundred cycles
         uint32_t run = 0u;
@@ -188,16 +213,17 @@ fine_sort_csr_kernel(const uint32_t* __restrict__ keys, const int32_t* __restric
         }
     }
     __syncthreads();
-    // row pointers of the tokens in this coarse bucket (key T: the invalid rows)
-    for (int f = threadIdx.x; f < F; f += kFineThreads) {
-        const int64_t t = (int64_t)c * F + f;
-        if (t <= T) ptr[t] = (int32_t)(lo + hist[f]);
+    if (PADDED) {  // row pointers of the tokens in this coarse bucket (key T: the invalid rows)
+        for (int f = threadIdx.x; f < F; f += kFineThreads) {
+            const int64_t t = (int64_t)c * F + f;
+            if (t <= T) ptr[t] = (int32_t)(lo + hist[f]);
+        }
     }
     const uint32_t lt = lanemask_lt();
     for (uint32_t base = lo; base < hi; base += kFineThreads) {
         const uint32_t i = base + threadIdx.x;
         const bool in = i < hi;
-        const int f = in ? (int)(keys[i] & fmask) : -1;
+        const int f = in ? (int)((keys[i] - kofs) & fmask) : -1;
         const uint32_t peers = __match_any_sync(0xffffffffu, f);
         const uint32_t below = __popc(peers & lt);
         const bool leader = in && below == 0u;
@@ -209,7 +235,7 @@ fine_sort_csr_kernel(const uint32_t* __restrict__ keys, const int32_t* __restric
             const uint32_t pos = lo + r;
             const int32_t o = idx[i];
             out_index[pos] = o;
-            ptid[pos] = si[o];
+            ptid[pos] = PADDED ? si[o] : (int32_t)(o / topk);
         }
         __syncthreads();
         if (leader) {
@@ -247,8 +273,9 @@ struct UnpermutePlan {
     bool probs, padded;
     // sort
     uint32_t key_range;  // number of distinct full keys
-    int fine_bits;       // padded beyond one pass: a pass on key >> fine_bits, then
-                         // fine_sort_csr_kernel (0: LSD passes or one pass)
+    int fine_bits;       // beyond one pass: a coarse pass on the key's high bits
+                         // (s = fine_bits), then fine_sort_kernel (0: LSD passes
+                         // or one pass)
     int passes;
     int shift[3];
     int bits[3];
@@ -329,18 +356,22 @@ static mr_status plan_unpermute(int64_t permutedRows, int64_t hidden, int32_t to
     const uint64_t range = paddedMode ? (uint64_t)T + 1 : (uint64_t)permutedRows + 1;
     p->key_range = (uint32_t)range;
     p->fine_bits = 0;
-    if (paddedMode && range > (UINT64_C(1) << kRadixDigitBits) &&
+    if (range > (UINT64_C(1) << kRadixDigitBits) &&
         range <= (UINT64_C(1) << (kRadixDigitBits + kMaxFineBits))) {
-        // padded: coarse counting sort on key >> s (257..4096 buckets), then
-        // one block per coarse bucket sorts by the low s bits and writes the CSR;
-        // s leaves about 2^9 coarse buckets while the fine keys fit a block
-        const int b = bits_for(range);
+        // two levels: a coarse counting sort on the key's high bits (about 2^9
+        // buckets, at most 4097), then one block per coarse bucket sorts by
+        // the low s bits, s <= kMaxFineBits so that the fine keys fit a block.
+        // Padded: digit key >> s over keys 0..T (the fine sort writes the CSR).
+        // Not padded: the valid keys 1..rows take digits 1 + (key - 1) >> s,
+        // the invalid key 0 digit 0.
+        const uint64_t span = paddedMode ? range : range - 1;  // keys split by s
+        const int b = bits_for(span);
         const int sbits = b - 9 < kMaxFineBits ? b - 9 : kMaxFineBits;
         p->fine_bits = sbits;
         p->passes = 1;
         p->shift[0] = sbits;
         p->bits[0] = kRadixDigitBits;
-        p->Bmax = (int)(((range - 1) >> sbits) + 1);
+        p->Bmax = (int)(((span - 1) >> sbits) + 1) + (paddedMode ? 0 : 1);
     } else if (range <= (UINT64_C(1) << kRadixDigitBits)) {
         p->passes = 1;
         p->shift[0] = 0;
@@ -538,14 +569,17 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
             const int B = p.fine_bits ? p.Bmax : p.passes == 1 ? (int)p.key_range : (1 << p.bits[pass]);
             const uint32_t mask = (p.passes == 1 || p.fine_bits)
                                       ? 0xffffffffu : (uint32_t)((1u << p.bits[pass]) - 1u);
-            RadixKey kf{sortedIndices, kin, limit, p.padded ? 1 : 0, p.shift[pass], mask};
+            RadixKey kf{sortedIndices, kin, limit, p.padded ? 1 : 0, p.shift[pass], mask,
+                        (p.fine_bits && !p.padded) ? 1 : 0};
             GroupListOut none{nullptr, nullptr, 0};
             const bool last = pass == p.passes - 1 && !p.fine_bits;
             PaddedProbs ppr{reinterpret_cast<const uint8_t*>(probs), nullptr, p.Eu, p.cap, p.pes};
             if (pass == 0 && p.padded && p.probs) ppr.pp = pp;
+            const bool apart = p.fine_bits && !p.padded;
             RadixScatter sc{kf, iin, keys[pass & 1], last ? nullptr : idx[pass & 1],
                             last ? outIndex : nullptr, last ? permuteTokenId : nullptr,
-                            p.topk > 0 ? p.topk : (int64_t)1, ppr};
+                            p.topk > 0 ? p.topk : (int64_t)1, ppr,
+                            apart ? outIndex : nullptr, apart ? permuteTokenId : nullptr};
             cudaError_t e;
             if (p.n <= kSortTile) {
                 e = csort_single_tile(kf, p.n, B, cs, none, sc, ss);  // one block
@@ -561,14 +595,17 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
         }
         if (p.fine_bits) {
             const size_t smem = (size_t)(2 + kFineWarps) * ((size_t)1 << p.fine_bits) * 4u;
+            auto kern = p.padded ? fine_sort_kernel<true> : fine_sort_kernel<false>;
             if (smem > 48 * 1024) {
-                cudaError_t e = cudaFuncSetAttribute(fine_sort_csr_kernel,
-                                                     cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+                cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
                 if (e != cudaSuccess) return e;
             }
-            return launch_pdl(fine_sort_csr_kernel, dim3((unsigned)p.Bmax), dim3(kFineThreads), smem, ss,
+            // not padded: coarse bucket 0 (the invalid entries) is already in place
+            const int blocks = p.padded ? p.Bmax : p.Bmax - 1;
+            return launch_pdl(kern, dim3((unsigned)blocks), dim3(kFineThreads), smem, ss,
                               (const uint32_t*)kin, (const int32_t*)iin, (const uint32_t*)cs.bucket_start,
-                              p.fine_bits, p.T, sortedIndices, outIndex, permuteTokenId, ptr);
+                              p.fine_bits, p.T, p.topk > 0 ? p.topk : (int64_t)1, sortedIndices, outIndex,
+                              permuteTokenId, ptr);
         }
         if (p.padded && p.passes > 1) {
             return launch_pdl(csr_from_keys_kernel, dim3(elementwise_grid(p.n + 1)), dim3(256), 0,
