@@ -56,7 +56,8 @@ def parse_args(argv=None):
                     help="attention workers (A) of the oracle's bounded sample (full workload: 256)")
     ap.add_argument("--small", action="store_true", help="a small case of the same workload (profiling)")
     ap.add_argument("--workload", choices=["roundtrip", "tiny", "topk", "int8", "padded", "context",
-                                           "batching", "permute", "permute_padded", "update_expert", "decode_unpermute"],
+                                           "batching", "permute", "permute_padded", "update_expert", "decode_unpermute",
+                                           "padded_slack"],
                     default="roundtrip",
                     help="roundtrip (the bench line) or one of the other workloads, timed per call "
                          "with an L2 flush before each")
@@ -683,14 +684,17 @@ def run_workload(args):
             u = w.make_unpermute_topk(**w.UNPERMUTE_TOPK)
         elif name == "decode_unpermute":
             u = w.make_unpermute_topk(**w.UNPERMUTE_DECODE)
+        elif name == "padded_slack":
+            u = w.make_unpermute_padded(**w.UNPERMUTE_PADDED_SLACK)
         else:
             u = w.make_unpermute_padded(**w.UNPERMUTE_PADDED)
         T, H, n, dt, pdt, Eu = u["T"], u["H"], u["n"], u["tokenDtype"], u["probsDtype"], u["Eu"]
         s, ps = w.ELEM_BYTES[dt], w.ELEM_BYTES[pdt]
         si = u["sortedIndices"].astype(np.int64)
         if u["padded"]:
+            # indices, prob lookups, the valid rows, the output, outIndex/permuteTokenId/permuteProbs
             V = int(((si >= 0) & (si < T)).sum())
-            alg = n * (4 + H * s + ps) + T * H * s + n * (8 + ps)
+            alg = n * (4 + ps) + V * H * s + T * H * s + n * (8 + ps)
         else:
             pr = u["probs"].reshape(T, Eu)
             pv = pr.T[(u["routingMap"] != 0).T]

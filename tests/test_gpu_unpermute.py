@@ -45,6 +45,11 @@ def test_padded_workload():
     check(w.make_unpermute_padded(**w.UNPERMUTE_PADDED))
 
 
+def test_padded_slack_workload():
+    """Capacity twice the routed load: half of the 131072 slots are padding."""
+    check(w.make_unpermute_padded(**w.UNPERMUTE_PADDED_SLACK))
+
+
 COMBOS = [(0, 0), (0, 3), (1, 1), (1, 3), (3, 3)]
 
 
@@ -136,6 +141,14 @@ SORT_CASES = {
                                                                probs_dtype=1, choices=(3, 8), seed=13),
     "two_level_wide_padded": lambda: w.make_unpermute_padded(T=32768, Eu=64, k=2, H=16, dtype=0,
                                                              probs_dtype=3, mult=7, seed=14),
+    # padded, the first key count past one pass (T = 4096: 4097 keys), and a
+    # token count that leaves the last coarse bucket part-filled (T = 5000,
+    # 32 fine keys) with slack capacity (padding slots)
+    "two_level_padded_4097_keys": lambda: w.make_unpermute_padded(T=4096, Eu=16, k=2, H=8, dtype=0,
+                                                                  probs_dtype=3, mult=5, seed=25),
+    "two_level_padded_ragged_slack": lambda: w.make_unpermute_padded(T=5000, Eu=8, k=2, H=8, dtype=1,
+                                                                     probs_dtype=3, mult=3, capacity=1500,
+                                                                     seed=24),
     # not padded, the first key count past one pass: 4096 rows, 3-bit fine keys
     "two_level_not_padded_4097_keys": lambda: w.make_unpermute_topk(T=1024, k=4, Eu=8, H=8, dtype=1,
                                                                     probs_dtype=1, choices=(1, 4), seed=21),

@@ -76,9 +76,10 @@ mask_scatter_kernel(const int8_t* __restrict__ map, const uint32_t* __restrict__
 // coarse pass followed by one block per coarse bucket).
 // Full key: not padded (invalid first) v+1 for 0 <= v < rows, else 0;
 //           padded (invalid last)      v   for 0 <= v < T,    else T.
-// The coarse digit of the not-padded two-level sort keeps the invalid entries
-// alone in bucket 0 (1 + (key - 1) >> shift for the others), so that their
-// final places are known after the coarse pass.
+// The coarse digit of the two-level sort keeps the invalid entries alone in a
+// bucket of their own, so that their final places are known after the coarse
+// pass: not padded, bucket 0 (1 + (key - 1) >> shift for the others); padded,
+// the last bucket (key >> shift for the others).
 // ---------------------------------------------------------------------------
 struct RadixKey {
     const int32_t* si;        // pass 0 source
@@ -87,7 +88,8 @@ struct RadixKey {
     int padded;
     int shift;
     uint32_t mask;
-    int coarse_invalid_apart;  // not padded, two levels: digit as described above
+    int coarse_invalid_apart;  // two levels: digit as described above
+    uint32_t invalid_bucket;   // padded, two levels: the last coarse bucket
     __device__ __forceinline__ uint32_t full(int64_t i) const {
         if (keys_in) return keys_in[i];
         const int32_t v = si[i];
@@ -96,7 +98,10 @@ struct RadixKey {
         return ok ? (uint32_t)v + 1u : 0u;
     }
     __device__ __forceinline__ int digit(uint32_t fk) const {
-        if (coarse_invalid_apart) return fk == 0u ? 0 : (int)(1u + ((fk - 1u) >> shift));
+        if (coarse_invalid_apart) {
+            if (padded) return fk == (uint32_t)limit ? (int)invalid_bucket : (int)(fk >> shift);
+            return fk == 0u ? 0 : (int)(1u + ((fk - 1u) >> shift));
+        }
         return (int)((fk >> shift) & mask);
     }
     __device__ __forceinline__ int operator()(int64_t i) const { return digit(full(i)); }
@@ -115,9 +120,9 @@ struct PaddedProbs {
 // and the item's original index move to d (every pass but the last); the last
 // pass writes outIndex and permuteTokenId instead. The first pass of a padded
 // sort with probs also writes permuteProbs[i]. In the coarse pass of the
-// not-padded two-level sort, an invalid entry (bucket 0, which starts at 0 and
-// keeps the original order) is already in its final place: it writes
-// outIndex and permuteTokenId at once (final_index, final_ptid).
+// two-level sort an invalid entry is already in its final place (its bucket,
+// first when not padded and last when padded, keeps the original order): it
+// writes outIndex and permuteTokenId at once (final_index, final_ptid).
 struct RadixScatter {
     RadixKey kf;
     const int32_t* idx_in;
@@ -141,9 +146,9 @@ struct RadixScatter {
         }
         const uint32_t fk = kf.full(i);
         const int32_t idx = idx_in ? idx_in[i] : (int32_t)i;
-        if (final_index && fk == 0u) {
+        if (final_index && fk == (kf.padded ? (uint32_t)kf.limit : 0u)) {
             final_index[d] = idx;
-            final_ptid[d] = (int32_t)(idx / topk);
+            final_ptid[d] = kf.padded ? kf.si[idx] : (int32_t)(idx / topk);
             return;
         }
         keys_out[d] = fk;
@@ -174,10 +179,12 @@ radix_scatter_kernel(RadixKey kf, int64_t n, int B, CsortBufs cs, RadixScatter s
 // ranked by key with warp matches, per-warp counters and a running count per
 // fine key.
 //   padded:     digit key >> s, fine key = key & (F-1); the fine starts are
-//               the CSR row pointers ptr[c*F + f]; permuteTokenId = the value.
-//   not padded: bucket 0 holds the invalid entries, placed by the coarse
-//               pass; block b sorts bucket b+1 by (key - 1) & (F-1);
+//               the CSR row pointers ptr[c*F + f] (the last block also writes
+//               ptr[T], the start of the invalid bucket that follows it);
+//               permuteTokenId = the value.
+//   not padded: block b sorts bucket b+1 by (key - 1) & (F-1);
 //               permuteTokenId = original index / topK.
+// The coarse pass has placed the invalid entries' bucket, which no block takes.
 constexpr int kFineThreads = 256;
 constexpr int kFineWarps = kFineThreads / 32;
 constexpr int kMaxFineBits = 10;
@@ -213,11 +220,12 @@ fine_sort_kernel(const uint32_t* __restrict__ keys, const int32_t* __restrict__ 
         }
     }
     __syncthreads();
-    if (PADDED) {  // row pointers of the tokens in this coarse bucket (key T: the invalid rows)
+    if (PADDED) {  // row pointers of the tokens in this coarse bucket
         for (int f = threadIdx.x; f < F; f += kFineThreads) {
             const int64_t t = (int64_t)c * F + f;
-            if (t <= T) ptr[t] = (int32_t)(lo + hist[f]);
+            if (t < T) ptr[t] = (int32_t)(lo + hist[f]);
         }
+        if (c == (int)gridDim.x - 1 && threadIdx.x == 0) ptr[T] = (int32_t)hi;
     }
     const uint32_t lt = lanemask_lt();
     for (uint32_t base = lo; base < hi; base += kFineThreads) {
@@ -358,20 +366,23 @@ static mr_status plan_unpermute(int64_t permutedRows, int64_t hidden, int32_t to
     p->fine_bits = 0;
     if (range > (UINT64_C(1) << kRadixDigitBits) &&
         range <= (UINT64_C(1) << (kRadixDigitBits + kMaxFineBits))) {
-        // two levels: a coarse counting sort on the key's high bits (about 2^9
-        // buckets, at most 4097), then one block per coarse bucket sorts by
-        // the low s bits, s <= kMaxFineBits so that the fine keys fit a block.
-        // Padded: digit key >> s over keys 0..T (the fine sort writes the CSR).
-        // Not padded: the valid keys 1..rows take digits 1 + (key - 1) >> s,
-        // the invalid key 0 digit 0.
-        const uint64_t span = paddedMode ? range : range - 1;  // keys split by s
+        // two levels: a coarse counting sort on the key's high bits (about 2^8
+        // buckets padded, 2^9 not padded -- the faster choices measured on
+        // GB300 -- and at most 4097), then one block per coarse bucket sorts
+        // by the low s bits, s <= kMaxFineBits so that the fine keys fit a
+        // block. The span = range - 1 valid keys take ((span - 1) >> s) + 1
+        // buckets and the invalid key one more (padded: the last, after the
+        // digits key >> s; not padded: bucket 0, before the digits
+        // 1 + (key - 1) >> s).
+        const uint64_t span = range - 1;
         const int b = bits_for(span);
-        const int sbits = b - 9 < kMaxFineBits ? b - 9 : kMaxFineBits;
+        const int coarse_bits = paddedMode ? 8 : 9;
+        const int sbits = b - coarse_bits < kMaxFineBits ? b - coarse_bits : kMaxFineBits;
         p->fine_bits = sbits;
         p->passes = 1;
         p->shift[0] = sbits;
         p->bits[0] = kRadixDigitBits;
-        p->Bmax = (int)(((span - 1) >> sbits) + 1) + (paddedMode ? 0 : 1);
+        p->Bmax = (int)(((span - 1) >> sbits) + 2);
     } else if (range <= (UINT64_C(1) << kRadixDigitBits)) {
         p->passes = 1;
         p->shift[0] = 0;
@@ -570,12 +581,12 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
             const uint32_t mask = (p.passes == 1 || p.fine_bits)
                                       ? 0xffffffffu : (uint32_t)((1u << p.bits[pass]) - 1u);
             RadixKey kf{sortedIndices, kin, limit, p.padded ? 1 : 0, p.shift[pass], mask,
-                        (p.fine_bits && !p.padded) ? 1 : 0};
+                        p.fine_bits ? 1 : 0, (uint32_t)(p.Bmax - 1)};
             GroupListOut none{nullptr, nullptr, 0};
             const bool last = pass == p.passes - 1 && !p.fine_bits;
             PaddedProbs ppr{reinterpret_cast<const uint8_t*>(probs), nullptr, p.Eu, p.cap, p.pes};
             if (pass == 0 && p.padded && p.probs) ppr.pp = pp;
-            const bool apart = p.fine_bits && !p.padded;
+            const bool apart = p.fine_bits != 0;
             RadixScatter sc{kf, iin, keys[pass & 1], last ? nullptr : idx[pass & 1],
                             last ? outIndex : nullptr, last ? permuteTokenId : nullptr,
                             p.topk > 0 ? p.topk : (int64_t)1, ppr,
@@ -600,8 +611,8 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
                 cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
                 if (e != cudaSuccess) return e;
             }
-            // not padded: coarse bucket 0 (the invalid entries) is already in place
-            const int blocks = p.padded ? p.Bmax : p.Bmax - 1;
+            // the invalid entries' bucket is already in place
+            const int blocks = p.Bmax - 1;
             return launch_pdl(kern, dim3((unsigned)blocks), dim3(kFineThreads), smem, ss,
                               (const uint32_t*)kin, (const int32_t*)iin, (const uint32_t*)cs.bucket_start,
                               p.fine_bits, p.T, p.topk > 0 ? p.topk : (int64_t)1, sortedIndices, outIndex,

@@ -201,19 +201,21 @@ def make_unpermute_topk(*, T: int, k: int, Eu: int, H: int, dtype: int, probs_dt
 
 
 def make_unpermute_padded(*, T: int, Eu: int, k: int, H: int, dtype: int, probs_dtype: int | None,
-                          mult: int = 37, seed: int = 3) -> dict:
+                          mult: int = 37, seed: int = 3, capacity: int | None = None) -> dict:
     """Padded (expert capacity) inputs with balanced routing: token t goes to
     experts (mult*t + (Eu/k)*j) mod Eu for j < k, so with Eu a power of two,
-    mult odd and T a multiple of Eu every expert gets capacity = T*k/Eu tokens.
-    sortedIndices[e*capacity + r] = r-th smallest token routed to e. probs =
-    Dirichlet(1) over the token's k experts (normalised Exp(1) draws)."""
+    mult odd and T a multiple of Eu every expert gets T*k/Eu tokens.
+    sortedIndices[e*capacity + r] = r-th smallest token routed to e, -1 in the
+    expert's unused slots; capacity = the largest expert load, or the given
+    capacity when larger (slack slots). probs = Dirichlet(1) over the token's k
+    experts (normalised Exp(1) draws)."""
     step = Eu // k
     routing = np.zeros((T, Eu), dtype=np.int8)
     t = np.arange(T)
     cols = np.stack([(mult * t + step * j) % Eu for j in range(k)], axis=1)  # [T, k]
     routing[t[:, None], cols] = 1
     counts = routing.sum(axis=0)
-    cap = int(counts.max())
+    cap = max(int(counts.max()), int(capacity or 0))
     sorted_idx = np.full(Eu * cap, -1, dtype=np.int32)
     e_idx, t_idx = np.nonzero(routing.T)            # expert-major, tokens ascending
     first = np.searchsorted(e_idx, np.arange(Eu))   # each expert's first pair
@@ -254,6 +256,8 @@ BATCHING_INT8_DECODE = dict(A=64, BS=32, K1=9, E=256, H=7168, dtype=DT_INT8, lay
                             micro=64, token_ids=True, seed=2)
 UNPERMUTE_TOPK = dict(T=4096, k=8, Eu=64, H=4096, dtype=DT_BF16, probs_dtype=DT_BF16, seed=1)
 UNPERMUTE_PADDED = dict(T=16384, Eu=128, k=4, H=4096, dtype=DT_F16, probs_dtype=DT_F32, seed=3)
+# the same routing with capacity twice the load: half of the expert slots are padding
+UNPERMUTE_PADDED_SLACK = dict(UNPERMUTE_PADDED, capacity=1024)
 # a decode-sized step: 64 tokens, each routed to 6-8 of 64 experts, H = 7168 bf16
 UNPERMUTE_DECODE = dict(T=64, k=8, Eu=64, H=7168, dtype=DT_BF16, probs_dtype=DT_BF16, seed=7)
 ROUNDTRIP_BATCHING = dict(A=256, BS=64, K1=9, E=1024, H=7168, dtype=DT_BF16, layerNum=4,
