@@ -27,7 +27,8 @@ __device__ __forceinline__ float ld_f32(const void* base, int64_t i) {
 constexpr int kListCap = 512;   // list entries per pass of the element-wise kernel
 constexpr int kRedUnroll = 4;   // rows in flight per warp step
 constexpr int kRedVQ = 2;       // 16-byte vectors per lane per hidden chunk
-constexpr int kRedRun = 2;      // hidden chunks per work unit (one slot-list read)
+constexpr int kRedRun = 2;      // hidden chunks per work unit (one slot-list read) when the
+                                // units of that length still fill the resident warps, else 1
 
 template <bool HAS_PROBS, bool PADDED, int PDT>
 __device__ __forceinline__ int build_list(int64_t c0, int64_t c1, const int32_t* __restrict__ si,
@@ -108,12 +109,13 @@ struct Vec<MR_DTYPE_F16> : Vec16<MR_DTYPE_F16> {};
 template <>
 struct Vec<MR_DTYPE_BF16> : Vec16<MR_DTYPE_BF16> {};
 
-// One warp per work item = (token, chunk of 32*kRedVQ 16-byte vectors of the
-// hidden dimension). The warp's lanes load up to 32 of the token's slots at a
-// time (index and weight), a ballot keeps the contributing ones in ascending
-// order, and the warp adds them kRedUnroll rows at a time, each lane owning
-// kRedVQ vectors: no shared memory and no block barrier.
-template <int TDT, int PDT, bool HAS_PROBS, bool PADDED>
+// One warp per work unit = (token, run of RUN consecutive chunks of 32*kRedVQ
+// 16-byte vectors of the hidden dimension). The warp's lanes load up to 32 of
+// the token's slots at a time (index and weight), a ballot keeps the
+// contributing ones in ascending order, and the warp adds them kRedUnroll rows
+// at a time, each lane owning kRedVQ vectors: no shared memory and no block
+// barrier.
+template <int TDT, int PDT, bool HAS_PROBS, bool PADDED, int RUN>
 __global__ void __launch_bounds__(256)
 unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows, int64_t row_bytes,
                              int64_t nvec, int64_t chunks, const int32_t* __restrict__ si,
@@ -123,16 +125,16 @@ unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows,
     using V = Vec<TDT>;
     pdl_enter();
     const int lane = threadIdx.x & 31;
-    // A work unit is a run of kRedRun consecutive hidden chunks of one token:
-    // the token's slot list is read once for the run.
-    const int64_t runs = (chunks + kRedRun - 1) / kRedRun;
+    // A work unit is a run of consecutive hidden chunks of one token: the
+    // token's slot list is read once for the run.
+    const int64_t runs = (chunks + RUN - 1) / RUN;
     const int64_t units = T * runs;
     const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
     for (int64_t unit = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; unit < units;
          unit += nw) {
         const int64_t t = unit / runs;
-        const int64_t c0 = (unit - t * runs) * kRedRun;
-        const int64_t c1 = c0 + kRedRun < chunks ? c0 + kRedRun : chunks;
+        const int64_t c0 = (unit - t * runs) * RUN;
+        const int64_t c1 = c0 + RUN < chunks ? c0 + RUN : chunks;
         int64_t L0, L1;
         if (PADDED) {
             L0 = ptr[t];

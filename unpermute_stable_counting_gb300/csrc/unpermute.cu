@@ -442,7 +442,7 @@ static cudaError_t launch_reduce(const UnpermutePlan& p, const uint8_t* permuted
         int bps = dev < 64 ? blocks_per_sm[dev] : 0;
         if (bps == 0) {
             if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                    &bps, unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED>, 256, 0) !=
+                    &bps, unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED, kRedRun>, 256, 0) !=
                     cudaSuccess || bps <= 0)
                 bps = 4;
             if (dev < 64) blocks_per_sm[dev] = bps;
@@ -451,9 +451,15 @@ static cudaError_t launch_reduce(const UnpermutePlan& p, const uint8_t* permuted
         const int64_t cap = (int64_t)device_sm_count() * bps;
         if (grid > cap) grid = cap;
         if (grid < 1) grid = 1;
-        return launch_kernel(pdl, unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED>, dim3((unsigned)grid),
-                          dim3(256), 0, s, permuted, p.rows, row_bytes, nvec, chunks, si, p.topk, pp,
-                          out_index, ptr, p.T, out);
+        // runs of kRedRun chunks share one slot-list read; when they would
+        // leave resident warps idle (a few tokens), one chunk per unit
+        // (measured on GB300: decode-sized call 22.8 -> 20.8 us; longer
+        // runs keep the padded reduce at 98 us instead of 106 us)
+        const int64_t long_units = p.T * ((chunks + kRedRun - 1) / kRedRun);
+        auto kern = long_units < cap * 8 ? unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED, 1>
+                                         : unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED, kRedRun>;
+        return launch_kernel(pdl, kern, dim3((unsigned)grid), dim3(256), 0, s, permuted, p.rows, row_bytes,
+                             nvec, chunks, si, p.topk, pp, out_index, ptr, p.T, out);
     }
     int64_t threads = p.H < 256 ? (p.H + 31) / 32 * 32 : 256;
     const int64_t gx = p.T < 0x7fffffff ? p.T : 0x7fffffff;
