@@ -213,6 +213,46 @@ def test_maximum_experts(padded):
     check(inp)
 
 
+SMALL_MAP_CASES = {
+    # T * Eu at the small-map limit (16384 entries: the weights are selected in
+    # the gather-reduce) and just past it (the maskedSelect kernels)
+    "at_limit": lambda: w.make_unpermute_topk(T=256, k=8, Eu=64, H=64, dtype=1, probs_dtype=1,
+                                              choices=(3, 8), seed=31),
+    "past_limit": lambda: w.make_unpermute_topk(T=257, k=8, Eu=64, H=64, dtype=1, probs_dtype=1,
+                                                choices=(3, 8), seed=32),
+    # more than 32 slots per token (several slot groups), fp32 probs with fp16 rows
+    "wide_topk": lambda: w.make_unpermute_topk(T=48, k=40, Eu=128, H=72, dtype=0, probs_dtype=3,
+                                               choices=(17, 40), seed=33),
+    # a wide map of few tokens: 4000 experts, the expert starts scanned in 16 steps
+    "many_experts": lambda: w.make_unpermute_topk(T=2, k=8, Eu=4000, H=8, dtype=1, probs_dtype=1,
+                                                  choices=(1, 8), seed=34),
+    # too wide for the 32 KB of shared memory (8192 experts): the maskedSelect kernels
+    "too_wide": lambda: w.make_unpermute_topk(T=1, k=8, Eu=8192, H=8, dtype=1, probs_dtype=1,
+                                              choices=(8,), seed=35),
+    # one token, one slot
+    "single": lambda: w.make_unpermute_topk(T=1, k=1, Eu=3, H=8, dtype=3, probs_dtype=3, choices=(1,),
+                                            seed=36),
+}
+
+
+@pytest.mark.parametrize("case", list(SMALL_MAP_CASES))
+def test_small_map_weights(case):
+    """Not padded with probs: the weights (and permuteProbs) selected by the
+    gather-reduce from a small routing map, at and around the size limits."""
+    check(SMALL_MAP_CASES[case]())
+
+
+def test_small_map_empty_and_invalid():
+    """An empty routing map (permuteProbs all 0, nothing added) and invalid
+    slot indices beside valid ones."""
+    inp = w.make_unpermute_topk(T=40, k=4, Eu=16, H=16, dtype=1, probs_dtype=1, choices=(2, 4), seed=37)
+    check(dict(inp, routingMap=np.zeros_like(inp["routingMap"])))
+    si = inp["sortedIndices"].copy()
+    si[::3] = -1
+    si[1::7] = inp["permutedRows"] + 5
+    check(dict(inp, sortedIndices=si))
+
+
 @pytest.mark.parametrize("T,Eu", [(8192, 64), (16384, 128)])
 def test_padded_invalid_rows_and_duplicates(T, Eu):
     """Two-level padded sort with 40% invalid rows (-1 and >= T: one fine

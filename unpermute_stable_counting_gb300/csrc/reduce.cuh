@@ -109,21 +109,128 @@ struct Vec<MR_DTYPE_F16> : Vec16<MR_DTYPE_F16> {};
 template <>
 struct Vec<MR_DTYPE_BF16> : Vec16<MR_DTYPE_BF16> {};
 
+// ---------------------------------------------------------------------------
+// Not padded, with probs, small routing map (T * Eu <= kSmallMapEntries): the
+// weight of slot i is permuteProbs[i], the i-th element of probs.T selected
+// by routingMap.T (expert-major, tokens ascending). Instead of the three
+// maskedSelect kernels, every block of the gather-reduce rebuilds that order
+// in shared memory -- 32-token column bitmasks and each expert's start -- and
+// finds slot i's element by rank: the expert whose range of starts holds i,
+// then the (i - start)-th routed token of its column. The warp that owns a
+// token's first hidden chunk also writes permuteProbs for the token's slots
+// (0 at and beyond the routed count).
+// ---------------------------------------------------------------------------
+constexpr int64_t kSmallMapEntries = 16384;
+
+struct SmallMap {
+    const int8_t* map;     // routingMap [T, Eu] (nullptr: weights come from pp)
+    const uint8_t* probs;  // probs [T, Eu], PDT
+    uint8_t* pp_out;       // permuteProbs [T * topk], PDT
+    int64_t Eu;
+};
+
+__host__ __device__ inline int64_t small_map_smem_words(int64_t T, int64_t Eu) {
+    return ((T + 31) / 32) * Eu + Eu + 1;  // bitmasks [nb][Eu], starts [Eu + 1]
+}
+
+// Every thread of the block takes part (block barriers and a block scan).
+__device__ __forceinline__ void small_map_build(const SmallMap& sm, int64_t T, uint32_t* smask,
+                                                uint32_t* sstart) {
+    __shared__ uint32_t wsum[32];
+    const int64_t Eu = sm.Eu;
+    const int64_t nb = (T + 31) / 32;
+    // one thread per (32-token block, expert) bitmask: 32 independent byte
+    // loads, consecutive experts on consecutive threads
+    for (int64_t item = threadIdx.x; item < nb * Eu; item += blockDim.x) {
+        const int64_t blk = item / Eu;
+        const int64_t e = item - blk * Eu;
+        const int64_t t0 = blk * 32;
+        int8_t m[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) m[j] = t0 + j < T ? sm.map[(t0 + j) * Eu + e] : (int8_t)0;
+        uint32_t bits = 0u;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) bits |= (m[j] != 0 ? 1u : 0u) << j;
+        smask[item] = bits;
+    }
+    __syncthreads();
+    uint32_t carry = 0u;
+    for (int64_t e0 = 0; e0 < Eu; e0 += blockDim.x) {  // exclusive scan of the column counts
+        const int64_t e = e0 + threadIdx.x;
+        uint32_t c = 0u;
+        if (e < Eu)
+            for (int64_t w = 0; w < nb; ++w) c += (uint32_t)__popc(smask[w * Eu + e]);
+        uint32_t tot = 0u;
+        const uint32_t x = block_exclusive_scan(c, wsum, &tot);
+        if (e < Eu) sstart[e] = carry + x;
+        carry += tot;
+    }
+    if (threadIdx.x == 0) sstart[Eu] = carry;
+    __syncthreads();
+}
+
+// permuteProbs[i]: its element of probs (src, -1 when i >= the routed count)
+// and its value.
+template <int PDT>
+__device__ __forceinline__ float small_map_weight(const SmallMap& sm, const uint32_t* smask,
+                                                  const uint32_t* sstart, int64_t i, int64_t& src) {
+    const int64_t Eu = sm.Eu;
+    if (i >= (int64_t)sstart[Eu]) {
+        src = -1;
+        return 0.0f;
+    }
+    int64_t lo = 0, hi = Eu;  // sstart[lo] <= i < sstart[hi]
+    while (hi - lo > 1) {
+        const int64_t mid = (lo + hi) >> 1;
+        if ((int64_t)sstart[mid] <= i) lo = mid;
+        else hi = mid;
+    }
+    uint32_t r = (uint32_t)(i - (int64_t)sstart[lo]);
+    int64_t w = 0;
+    uint32_t m = smask[lo];
+    uint32_t c = (uint32_t)__popc(m);
+    while (r >= c) {  // the column holds more than r routed tokens
+        r -= c;
+        ++w;
+        m = smask[w * Eu + lo];
+        c = (uint32_t)__popc(m);
+    }
+    for (uint32_t k = 0; k < r; ++k) m &= m - 1u;  // drop the r lower set bits
+    src = (w * 32 + (__ffs(m) - 1)) * Eu + lo;
+    return ld_f32<PDT>(sm.probs, src);
+}
+
+template <int PDT>
+__device__ __forceinline__ void small_map_store(const SmallMap& sm, int64_t i, int64_t src) {
+    if (PDT == MR_DTYPE_F32) {
+        reinterpret_cast<uint32_t*>(sm.pp_out)[i] =
+            src < 0 ? 0u : __ldg(reinterpret_cast<const uint32_t*>(sm.probs) + src);
+    } else {
+        reinterpret_cast<uint16_t*>(sm.pp_out)[i] =
+            src < 0 ? (uint16_t)0 : __ldg(reinterpret_cast<const unsigned short*>(sm.probs) + src);
+    }
+}
+
 // One warp per work unit = (token, run of RUN consecutive chunks of 32*kRedVQ
 // 16-byte vectors of the hidden dimension). The warp's lanes load up to 32 of
 // the token's slots at a time (index and weight), a ballot keeps the
 // contributing ones in ascending order, and the warp adds them kRedUnroll rows
-// at a time, each lane owning kRedVQ vectors: no shared memory and no block
-// barrier.
-template <int TDT, int PDT, bool HAS_PROBS, bool PADDED, int RUN>
+// at a time, each lane owning kRedVQ vectors: no block barrier after the
+// start, and shared memory only for the small-map weights (SMALL).
+template <int TDT, int PDT, bool HAS_PROBS, bool PADDED, int RUN, bool SMALL>
 __global__ void __launch_bounds__(256)
 unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows, int64_t row_bytes,
                              int64_t nvec, int64_t chunks, const int32_t* __restrict__ si,
                              int64_t topk, const void* __restrict__ pp,
                              const int32_t* __restrict__ out_index, const int32_t* __restrict__ ptr,
-                             int64_t T, uint8_t* __restrict__ out) {
+                             int64_t T, uint8_t* __restrict__ out, SmallMap smap) {
     using V = Vec<TDT>;
+    static_assert(!SMALL || (HAS_PROBS && !PADDED), "small-map weights are for the not-padded probs branch");
+    extern __shared__ __align__(16) uint32_t red_smem[];
+    uint32_t* smask = red_smem;
+    uint32_t* sstart = red_smem + ((T + 31) / 32) * smap.Eu;
     pdl_enter();
+    if constexpr (SMALL) small_map_build(smap, T, smask, sstart);
     const int lane = threadIdx.x & 31;
     // A work unit is a run of consecutive hidden chunks of one token: the
     // token's slot list is read once for the run.
@@ -159,7 +266,15 @@ unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows,
                     keep0 = v >= 0 && (int64_t)v < rows;
                     r = v;
                 }
-                if (HAS_PROBS && keep0) {
+                if constexpr (SMALL) {
+                    int64_t src;
+                    const float ws = small_map_weight<PDT>(smap, smask, sstart, e, src);
+                    if (c0 == 0) small_map_store<PDT>(smap, e, src);
+                    if (keep0) {
+                        w0 = ws;
+                        keep0 = w0 != 0.0f;
+                    }
+                } else if (HAS_PROBS && keep0) {
                     w0 = ld_f32<PDT>(pp, PADDED ? r : e);
                     keep0 = w0 != 0.0f;
                 }
@@ -194,7 +309,15 @@ unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows,
                         keep = v >= 0 && (int64_t)v < rows;
                         r = v;
                     }
-                    if (HAS_PROBS && keep) {
+                    if constexpr (SMALL) {
+                        int64_t src;
+                        const float ws = small_map_weight<PDT>(smap, smask, sstart, e, src);
+                        if (c == 0) small_map_store<PDT>(smap, e, src);
+                        if (keep) {
+                            w = ws;
+                            keep = w != 0.0f;
+                        }
+                    } else if (HAS_PROBS && keep) {
                         w = ld_f32<PDT>(pp, PADDED ? r : e);
                         keep = w != 0.0f;
                     }

@@ -6,7 +6,8 @@
 //
 // Launch sequence on the caller's stream (PDL-chained):
 //   not padded, probs : maskedSelect = column bitmasks -> csort prefix ->
-//                       scatter (+ zero tail)
+//                       scatter (+ zero tail); for a small routing map the
+//                       gather-reduce selects the weights itself instead
 //   always            : stable sort of sortedIndices -> outIndex,
 //                       permuteTokenId: one pass of the counting-sort engine
 //                       up to 4096 keys; up to 2^22 keys a coarse pass on
@@ -425,41 +426,70 @@ static int elementwise_grid(int64_t n) {
     return (int)(want < 1 ? 1 : (want < cap ? want : cap));
 }
 
+// Whether the gather-reduce takes the 16-byte vector path (row bytes and
+// buffers 16-byte aligned); the element-wise kernel serves the rest.
+static bool reduce_vec_ok(const UnpermutePlan& p, const void* permuted, const void* out) {
+    return (p.H * p.es) % 16 == 0 && reinterpret_cast<uintptr_t>(permuted) % 16 == 0 &&
+           reinterpret_cast<uintptr_t>(out) % 16 == 0;
+}
+
+// Not padded with probs: whether the gather-reduce derives the weights from a
+// small routing map itself (SmallMap), instead of the maskedSelect kernels.
+static bool use_small_map(const UnpermutePlan& p, const void* permuted, const void* out) {
+    return p.probs && !p.padded && p.T * p.Eu <= kSmallMapEntries &&
+           small_map_smem_words(p.T, p.Eu) * 4 <= 32 * 1024 && reduce_vec_ok(p, permuted, out);
+}
+
+template <int TDT, int PDT, bool HAS_PROBS, bool PADDED, bool SMALL>
+static cudaError_t launch_reduce_vec(const UnpermutePlan& p, const uint8_t* permuted,
+                                     const int32_t* si, const void* pp, const int32_t* out_index,
+                                     const int32_t* ptr, uint8_t* out, const SmallMap& smap,
+                                     cudaStream_t s, bool pdl) {
+    const int64_t row_bytes = p.H * p.es;
+    const int64_t nvec = row_bytes / 16;
+    const int64_t chunks = (nvec + 32 * kRedVQ - 1) / (32 * kRedVQ);
+    const int64_t warps = p.T * chunks;
+    const size_t smem = SMALL ? (size_t)small_map_smem_words(p.T, p.Eu) * 4u : 0u;
+    static int blocks_per_sm[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int bps = dev < 64 ? blocks_per_sm[dev] : 0;
+    if (bps == 0) {
+        // registers set the occupancy (the small-map shared memory is at most 32 KB)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &bps, unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED, kRedRun, SMALL>, 256, 0) !=
+                cudaSuccess || bps <= 0)
+            bps = 4;
+        if (dev < 64) blocks_per_sm[dev] = bps;
+    }
+    int64_t grid = (warps + 7) / 8;
+    const int64_t cap = (int64_t)device_sm_count() * bps;
+    if (grid > cap) grid = cap;
+    if (grid < 1) grid = 1;
+    // runs of kRedRun chunks share one slot-list read; when they would
+    // leave resident warps idle (a few tokens), one chunk per unit
+    // (measured on GB300: decode-sized call 22.8 -> 20.8 us; longer
+    // runs keep the padded reduce at 98 us instead of 106 us)
+    const int64_t long_units = p.T * ((chunks + kRedRun - 1) / kRedRun);
+    auto kern = long_units < cap * 8 ? unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED, 1, SMALL>
+                                     : unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED, kRedRun, SMALL>;
+    return launch_kernel(pdl, kern, dim3((unsigned)grid), dim3(256), smem, s, permuted, p.rows, row_bytes,
+                         nvec, chunks, si, p.topk, pp, out_index, ptr, p.T, out, smap);
+}
+
 template <int TDT, int PDT, bool HAS_PROBS, bool PADDED>
 static cudaError_t launch_reduce(const UnpermutePlan& p, const uint8_t* permuted,
                                  const int32_t* si, const void* pp, const int32_t* out_index,
-                                 const int32_t* ptr, uint8_t* out, cudaStream_t s, bool pdl) {
-    const int64_t row_bytes = p.H * p.es;
-    const bool vec_ok = (row_bytes % 16 == 0) && (reinterpret_cast<uintptr_t>(permuted) % 16 == 0) &&
-                        (reinterpret_cast<uintptr_t>(out) % 16 == 0);
-    if (vec_ok) {
-        const int64_t nvec = row_bytes / 16;
-        const int64_t chunks = (nvec + 32 * kRedVQ - 1) / (32 * kRedVQ);
-        const int64_t warps = p.T * chunks;
-        static int blocks_per_sm[64] = {0};
-        int dev = 0;
-        cudaGetDevice(&dev);
-        int bps = dev < 64 ? blocks_per_sm[dev] : 0;
-        if (bps == 0) {
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                    &bps, unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED, kRedRun>, 256, 0) !=
-                    cudaSuccess || bps <= 0)
-                bps = 4;
-            if (dev < 64) blocks_per_sm[dev] = bps;
+                                 const int32_t* ptr, uint8_t* out, const SmallMap& smap,
+                                 cudaStream_t s, bool pdl) {
+    if (reduce_vec_ok(p, permuted, out)) {
+        if constexpr (HAS_PROBS && !PADDED) {
+            if (smap.map)
+                return launch_reduce_vec<TDT, PDT, HAS_PROBS, PADDED, true>(p, permuted, si, pp, out_index,
+                                                                           ptr, out, smap, s, pdl);
         }
-        int64_t grid = (warps + 7) / 8;
-        const int64_t cap = (int64_t)device_sm_count() * bps;
-        if (grid > cap) grid = cap;
-        if (grid < 1) grid = 1;
-        // runs of kRedRun chunks share one slot-list read; when they would
-        // leave resident warps idle (a few tokens), one chunk per unit
-        // (measured on GB300: decode-sized call 22.8 -> 20.8 us; longer
-        // runs keep the padded reduce at 98 us instead of 106 us)
-        const int64_t long_units = p.T * ((chunks + kRedRun - 1) / kRedRun);
-        auto kern = long_units < cap * 8 ? unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED, 1>
-                                         : unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED, kRedRun>;
-        return launch_kernel(pdl, kern, dim3((unsigned)grid), dim3(256), 0, s, permuted, p.rows, row_bytes,
-                             nvec, chunks, si, p.topk, pp, out_index, ptr, p.T, out);
+        return launch_reduce_vec<TDT, PDT, HAS_PROBS, PADDED, false>(p, permuted, si, pp, out_index, ptr,
+                                                                    out, smap, s, pdl);
     }
     int64_t threads = p.H < 256 ? (p.H + 31) / 32 * 32 : 256;
     const int64_t gx = p.T < 0x7fffffff ? p.T : 0x7fffffff;
@@ -471,13 +501,14 @@ static cudaError_t launch_reduce(const UnpermutePlan& p, const uint8_t* permuted
 template <int TDT, int PDT>
 static cudaError_t dispatch_reduce(const UnpermutePlan& p, const uint8_t* permuted,
                                    const int32_t* si, const void* pp, const int32_t* out_index,
-                                   const int32_t* ptr, uint8_t* out, cudaStream_t s, bool pdl) {
+                                   const int32_t* ptr, uint8_t* out, const SmallMap& smap,
+                                   cudaStream_t s, bool pdl) {
     if (p.probs) {
-        return p.padded ? launch_reduce<TDT, PDT, true, true>(p, permuted, si, pp, out_index, ptr, out, s, pdl)
-                        : launch_reduce<TDT, PDT, true, false>(p, permuted, si, pp, out_index, ptr, out, s, pdl);
+        return p.padded ? launch_reduce<TDT, PDT, true, true>(p, permuted, si, pp, out_index, ptr, out, smap, s, pdl)
+                        : launch_reduce<TDT, PDT, true, false>(p, permuted, si, pp, out_index, ptr, out, smap, s, pdl);
     }
-    return p.padded ? launch_reduce<TDT, PDT, false, true>(p, permuted, si, pp, out_index, ptr, out, s, pdl)
-                    : launch_reduce<TDT, PDT, false, false>(p, permuted, si, pp, out_index, ptr, out, s, pdl);
+    return p.padded ? launch_reduce<TDT, PDT, false, true>(p, permuted, si, pp, out_index, ptr, out, smap, s, pdl)
+                    : launch_reduce<TDT, PDT, false, false>(p, permuted, si, pp, out_index, ptr, out, smap, s, pdl);
 }
 
 }  // namespace mr
@@ -525,9 +556,15 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
     uint8_t* wp = reinterpret_cast<uint8_t*>(workspace);
     uint8_t* pp = reinterpret_cast<uint8_t*>(permuteProbs);
 
+    // A small routing map (not padded, with probs): the gather-reduce selects
+    // the weights from it itself and writes permuteProbs (SmallMap).
+    SmallMap smap{nullptr, nullptr, nullptr, 0};
+    if (use_small_map(p, permutedTokens, unpermutedTokens))
+        smap = SmallMap{routingMap, reinterpret_cast<const uint8_t*>(probs), pp, p.Eu};
+
     // ---- permuteProbs (maskedSelect or the padded lookup) --------------------
     auto launch_probs = [&](cudaStream_t ss) -> cudaError_t {
-        if (p.probs && !p.padded) {
+        if (p.probs && !p.padded && !smap.map) {
             const int64_t nblk = (p.T + 31) / 32;
             const int64_t items = nblk * p.Eu;
             uint8_t* q = wp;
@@ -637,15 +674,15 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
     auto launch_reduce_any = [&](cudaStream_t ss, bool pdl) -> cudaError_t {
         switch (p.tdt * 4 + p.pdt) {
             case MR_DTYPE_F16 * 4 + MR_DTYPE_F16:
-                return dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss, pdl);
+                return dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, pdl);
             case MR_DTYPE_F16 * 4 + MR_DTYPE_F32:
-                return dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss, pdl);
+                return dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, pdl);
             case MR_DTYPE_BF16 * 4 + MR_DTYPE_BF16:
-                return dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_BF16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss, pdl);
+                return dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_BF16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, pdl);
             case MR_DTYPE_BF16 * 4 + MR_DTYPE_F32:
-                return dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss, pdl);
+                return dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, pdl);
             case MR_DTYPE_F32 * 4 + MR_DTYPE_F32:
-                return dispatch_reduce<MR_DTYPE_F32, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, ss, pdl);
+                return dispatch_reduce<MR_DTYPE_F32, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, pdl);
         }
         return cudaErrorInvalidValue;
     };
