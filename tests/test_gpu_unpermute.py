@@ -232,13 +232,20 @@ SMALL_MAP_CASES = {
     # one token, one slot
     "single": lambda: w.make_unpermute_topk(T=1, k=1, Eu=3, H=8, dtype=3, probs_dtype=3, choices=(1,),
                                             seed=36),
+    # past the small-map limit (the maskedSelect kernels): more than 32 slots
+    # per token, and several units per warp with runs of two chunks
+    "wide_topk_past_limit": lambda: w.make_unpermute_topk(T=600, k=40, Eu=128, H=72, dtype=0, probs_dtype=3,
+                                                      choices=(9, 40), seed=38),
+    "runs_past_limit": lambda: w.make_unpermute_topk(T=3000, k=6, Eu=48, H=2048, dtype=1, probs_dtype=3,
+                                                 choices=(2, 6), seed=39),
 }
 
 
 @pytest.mark.parametrize("case", list(SMALL_MAP_CASES))
 def test_small_map_weights(case):
     """Not padded with probs: the weights (and permuteProbs) selected by the
-    gather-reduce from a small routing map, at and around the size limits."""
+    gather-reduce from a small routing map, at and around the size limits,
+    and larger maps through the maskedSelect kernels."""
     check(SMALL_MAP_CASES[case]())
 
 
