@@ -236,6 +236,12 @@ SMALL_MAP_CASES = {
     # per token, and several units per warp with runs of two chunks
     "wide_topk_past_limit": lambda: w.make_unpermute_topk(T=600, k=40, Eu=128, H=72, dtype=0, probs_dtype=3,
                                                       choices=(9, 40), seed=38),
+    # the one-kernel maskedSelect at its limit (4096 tiles of 1024 map entries)
+    # and past it (column bitmasks, prefix and scatter kernels)
+    "one_kernel_select_at_limit": lambda: w.make_unpermute_topk(T=65536, k=2, Eu=64, H=8, dtype=1,
+                                                                probs_dtype=1, choices=(1, 2), seed=40),
+    "select_chain_past_limit": lambda: w.make_unpermute_topk(T=65600, k=2, Eu=64, H=8, dtype=1,
+                                                             probs_dtype=3, choices=(1, 2), seed=41),
     "runs_past_limit": lambda: w.make_unpermute_topk(T=3000, k=6, Eu=48, H=2048, dtype=1, probs_dtype=3,
                                                  choices=(2, 6), seed=39),
 }
@@ -244,8 +250,9 @@ SMALL_MAP_CASES = {
 @pytest.mark.parametrize("case", list(SMALL_MAP_CASES))
 def test_small_map_weights(case):
     """Not padded with probs: the weights (and permuteProbs) selected by the
-    gather-reduce from a small routing map, at and around the size limits,
-    and larger maps through the maskedSelect kernels."""
+    gather-reduce from a small routing map, at and around the size limits;
+    larger maps through the one-kernel maskedSelect, and past its limit the
+    three-kernel one."""
     check(SMALL_MAP_CASES[case]())
 
 

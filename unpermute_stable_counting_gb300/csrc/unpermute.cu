@@ -5,9 +5,12 @@
 // prob != 0 skip, fp32 Cast/Muls/Add and the CAST_RINT back-cast).
 //
 // Launch sequence on the caller's stream (PDL-chained):
-//   not padded, probs : maskedSelect = column bitmasks -> csort prefix ->
-//                       scatter (+ zero tail); for a small routing map the
-//                       gather-reduce selects the weights itself instead
+//   not padded, probs : maskedSelect: one cooperative kernel (counts per
+//                       tile, a grid barrier, the scatter and zero tail) up
+//                       to 4096 tiles of 1024 map entries, else column
+//                       bitmasks -> csort prefix -> scatter; for a small
+//                       routing map the gather-reduce selects the weights
+//                       itself instead
 //   always            : stable sort of sortedIndices -> outIndex,
 //                       permuteTokenId: one pass of the counting-sort engine
 //                       up to 4096 keys; up to 2^22 keys a coarse pass on
@@ -28,10 +31,13 @@
 #include <cstdlib>
 #include <mutex>
 
+#include <cooperative_groups.h>
+
 #include "reduce.cuh"
 #include "routing.cuh"
 
 namespace mr {
+namespace cg = cooperative_groups;
 
 // Copy one element of 2 or 4 bytes (the probs dtype) without interpreting it.
 __device__ __forceinline__ void copy_prob(uint8_t* dst, int64_t di, const uint8_t* src, int64_t si,
@@ -70,6 +76,85 @@ mask_scatter_kernel(const int8_t* __restrict__ map, const uint32_t* __restrict__
         }
         if (i >= nnz && i < n) zero_prob(pp, i, pes);
     }
+}
+
+// One-kernel maskedSelect (not padded, with probs) for maps of at most
+// kMsMaxTiles tiles: the routed elements of probs.T in expert-major order
+// (f = e*T + t, tokens ascending within an expert). Tiles of kMsTile
+// consecutive f; each block counts the routed entries of its tiles, a grid
+// barrier (cooperative launch: every block resident), then each block sums
+// the counts of the lower tiles and scatters its tiles' probs; positions at
+// and beyond the routed count are zeroed.
+constexpr int kMsThreads = 256;
+constexpr int kMsPer = 4;
+constexpr int64_t kMsTile = (int64_t)kMsThreads * kMsPer;
+constexpr int64_t kMsMaxTiles = 4096;
+
+__global__ void __launch_bounds__(kMsThreads)
+mask_select_kernel(const int8_t* __restrict__ map, int64_t T, int64_t Eu, int64_t n,
+                   const uint8_t* __restrict__ probs, int pes, uint32_t* __restrict__ tile_cnt,
+                   uint8_t* __restrict__ pp) {
+    __shared__ uint32_t wsum[32];
+    cg::grid_group grid = cg::this_grid();
+    const int64_t N = T * Eu;
+    const int64_t ntiles = (N + kMsTile - 1) / kMsTile;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        const int64_t f0 = tile * kMsTile + (int64_t)threadIdx.x * kMsPer;
+        int64_t e = f0 / T, t = f0 - e * T;
+        int8_t m[kMsPer];
+#pragma unroll
+        for (int q = 0; q < kMsPer; ++q) {
+            m[q] = f0 + q < N ? map[t * Eu + e] : (int8_t)0;
+            if (++t == T) { t = 0; ++e; }
+        }
+        uint32_t c = 0u;
+#pragma unroll
+        for (int q = 0; q < kMsPer; ++q) c += m[q] != 0 ? 1u : 0u;
+        uint32_t tot = 0u;
+        block_exclusive_scan(c, wsum, &tot);
+        if (threadIdx.x == 0) tile_cnt[tile] = tot;
+    }
+    grid.sync();
+    // total routed count, and the blocks' tile prefixes
+    uint32_t nnz = 0u;
+    {
+        uint32_t s = 0u;
+        for (int64_t u = threadIdx.x; u < ntiles; u += kMsThreads) s += __ldcg(&tile_cnt[u]);
+        block_exclusive_scan(s, wsum, &nnz);
+    }
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        uint32_t below = 0u;
+        {
+            uint32_t s = 0u;
+            for (int64_t u = threadIdx.x; u < tile; u += kMsThreads) s += __ldcg(&tile_cnt[u]);
+            block_exclusive_scan(s, wsum, &below);
+        }
+        const int64_t f0 = tile * kMsTile + (int64_t)threadIdx.x * kMsPer;
+        int64_t e = f0 / T, t = f0 - e * T;
+        int64_t src[kMsPer];
+        uint32_t c = 0u;
+#pragma unroll
+        for (int q = 0; q < kMsPer; ++q) {
+            src[q] = -1;
+            if (f0 + q < N && map[t * Eu + e] != 0) {
+                src[q] = t * Eu + e;
+                ++c;
+            }
+            if (++t == T) { t = 0; ++e; }
+        }
+        uint32_t tot = 0u;
+        uint32_t pos = below + block_exclusive_scan(c, wsum, &tot);
+#pragma unroll
+        for (int q = 0; q < kMsPer; ++q) {
+            if (src[q] >= 0) {
+                if ((int64_t)pos < n) copy_prob(pp, pos, probs, src[q], pes);
+                ++pos;
+            }
+        }
+    }
+    const int64_t stride = (int64_t)gridDim.x * kMsThreads;
+    for (int64_t i = (int64_t)nnz + (int64_t)blockIdx.x * kMsThreads + threadIdx.x; i < n; i += stride)
+        zero_prob(pp, i, pes);
 }
 
 // ---------------------------------------------------------------------------
@@ -564,6 +649,35 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
 
     // ---- permuteProbs (maskedSelect or the padded lookup) --------------------
     auto launch_probs = [&](cudaStream_t ss) -> cudaError_t {
+        const int64_t ms_tiles = (p.T * p.Eu + kMsTile - 1) / kMsTile;
+        if (p.probs && !p.padded && !smap.map && ms_tiles <= kMsMaxTiles) {
+            static int ms_bps[64] = {0};
+            int dev = 0;
+            cudaGetDevice(&dev);
+            int bps = dev < 64 ? ms_bps[dev] : 0;
+            if (bps == 0) {
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, mask_select_kernel, kMsThreads, 0) !=
+                        cudaSuccess || bps <= 0)
+                    return cudaErrorInvalidConfiguration;
+                if (dev < 64) ms_bps[dev] = bps;
+            }
+            int64_t grid = (int64_t)device_sm_count() * bps;
+            if (grid > ms_tiles) grid = ms_tiles;
+            if (grid < 1) grid = 1;
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)grid);
+            cfg.blockDim = dim3(kMsThreads);
+            cfg.dynamicSmemBytes = 0;
+            cfg.stream = ss;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeCooperative;
+            attr[0].val.cooperative = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            return cudaLaunchKernelEx(&cfg, mask_select_kernel, routingMap, p.T, p.Eu, p.n,
+                                      reinterpret_cast<const uint8_t*>(probs), p.pes,
+                                      reinterpret_cast<uint32_t*>(wp), pp);
+        }
         if (p.probs && !p.padded && !smap.map) {
             const int64_t nblk = (p.T + 31) / 32;
             const int64_t items = nblk * p.Eu;
