@@ -112,8 +112,8 @@ struct Vec<MR_DTYPE_BF16> : Vec16<MR_DTYPE_BF16> {};
 // ---------------------------------------------------------------------------
 // Not padded, with probs, small routing map (T * Eu <= kSmallMapEntries): the
 // weight of slot i is permuteProbs[i], the i-th element of probs.T selected
-// by routingMap.T (expert-major, tokens ascending). Instead of the three
-// maskedSelect kernels, every block of the gather-reduce rebuilds that order
+// by routingMap.T (expert-major, tokens ascending). Instead of a separate
+// maskedSelect, every block of the gather-reduce rebuilds that order
 // in shared memory -- 32-token column bitmasks and each expert's start -- and
 // finds slot i's element by rank: the expert whose range of starts holds i,
 // then the (i - start)-th routed token of its column. The warp that owns a

@@ -96,6 +96,7 @@ mask_select_kernel(const int8_t* __restrict__ map, int64_t T, int64_t Eu, int64_
                    uint8_t* __restrict__ pp) {
     __shared__ uint32_t wsum[32];
     cg::grid_group grid = cg::this_grid();
+    pdl_enter();  // launched in plain stream order (cooperative): returns at once
     const int64_t N = T * Eu;
     const int64_t ntiles = (N + kMsTile - 1) / kMsTile;
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
