@@ -559,6 +559,19 @@ static cudaError_t launch_reduce_vec(const UnpermutePlan& p, const uint8_t* perm
     const int64_t long_units = p.T * ((chunks + kRedRun - 1) / kRedRun);
     auto kern = long_units < cap * 8 ? unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED, 1, SMALL>
                                      : unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED, kRedRun, SMALL>;
+    if (!pdl) {
+        // A short reduce launched in plain order has the index sort running
+        // beside it on the (higher-priority) auxiliary stream: one work unit
+        // per warp, so that blocks retire as they finish and the sort's blocks
+        // take the freed slots, instead of a persistent grid that holds every
+        // SM until its end (measured on GB300: top-k T=4096, k=8, H=4096
+        // 55.6 -> 53.5 us; the reduce itself 41 -> 43 us)
+        const int64_t run = long_units < cap * 8 ? 1 : kRedRun;
+        const int64_t units = p.T * ((chunks + run - 1) / run);
+        grid = (units + 7) / 8;
+        if (grid > 0x7fffffff) grid = 0x7fffffff;
+        if (grid < 1) grid = 1;
+    }
     return launch_kernel(pdl, kern, dim3((unsigned)grid), dim3(256), smem, s, permuted, p.rows, row_bytes,
                          nvec, chunks, si, p.topk, pp, out_index, ptr, p.T, out, smap);
 }
@@ -826,10 +839,11 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
             // Under PDL the persistent reduce takes the SMs while it waits for
             // the probs, and the concurrent sort then runs on what is left.
             // A short reduce would end up waiting for the sort at the join,
-            // so it is launched in plain stream order; a long one (here more
-            // than 1 GB of rows, ~150 us) hides the sort either way and keeps
-            // the launch overlap (measured on GB300: top-k T=4096, k=8, H=4096
-            // 75.7 -> 55.6 us; the 2.1 GB round trip 0.989 vs 0.995 ms)
+            // so it is launched in plain stream order (with a non-persistent
+            // grid, see launch_reduce_vec); a long one (here more than 1 GB of
+            // rows, ~150 us) hides the sort either way and keeps the launch
+            // overlap (measured on GB300: top-k T=4096, k=8, H=4096 75.7 ->
+            // 55.6 us; the 2.1 GB round trip 0.989 vs 0.995 ms)
             const double reduce_bytes = (double)p.T * (double)p.topk * (double)p.H * p.es;
             e = launch_reduce_any(s, reduce_bytes > kPdlReduceBytes);
             profile_mark(s, 7);
