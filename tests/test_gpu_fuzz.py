@@ -72,6 +72,30 @@ def test_unpermute_random(case):
     assert_unpermute_equal(got, ref, inp)
 
 
+@pytest.mark.parametrize("case", range(16))
+def test_unpermute_random_mid_maps(case):
+    """Not padded with probs, routing maps of 16K-800K entries: the one-kernel
+    maskedSelect (and the small-map path below its limit), random dtypes, hidden
+    sizes, slot counts and invalid slots."""
+    r = np.random.default_rng(5000 + case)
+    dt = int(r.choice([0, 1, 3]))
+    pdt = dt if r.integers(0, 2) else 3
+    T = int(r.integers(100, 3001))
+    k = int(r.choice([1, 2, 4, 8, 9]))
+    Eu = int(r.integers(max(k, 8), 257))
+    H = int(r.choice([7, 8, 64, 136, 520]))  # 7: the element-wise reduce
+    inp = w.make_unpermute_topk(T=T, k=k, Eu=Eu, H=H, dtype=dt, probs_dtype=pdt,
+                                choices=tuple(sorted({1, (k + 1) // 2, k})), seed=case)
+    if r.integers(0, 2):
+        si = inp["sortedIndices"].copy()
+        bad = r.random(si.size) < 0.1
+        si[bad] = r.choice([-1, inp["permutedRows"]], size=int(bad.sum())).astype(np.int32)
+        inp = dict(inp, sortedIndices=si)
+    ref = oracle.unpermute(inp)
+    got = unpermute_numpy(run_unpermute(inp), inp)
+    assert_unpermute_equal(got, ref, inp)
+
+
 @pytest.mark.parametrize("case", range(32))
 def test_permute_random(case):
     r = np.random.default_rng(3000 + case)
