@@ -610,6 +610,37 @@ static cudaError_t dispatch_reduce(const UnpermutePlan& p, const uint8_t* permut
                     : launch_reduce<TDT, PDT, false, false>(p, permuted, si, pp, out_index, ptr, out, smap, s, pdl);
 }
 
+// The one-kernel maskedSelect: a cooperative launch (every block resident for
+// its grid barrier) of at most the resident blocks, and no more than the tiles.
+static cudaError_t launch_mask_select(const UnpermutePlan& p, const int8_t* map, const uint8_t* probs,
+                                      uint32_t* tile_cnt, uint8_t* pp, cudaStream_t s) {
+    static int blocks_per_sm[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int bps = dev < 64 ? blocks_per_sm[dev] : 0;
+    if (bps == 0) {
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, mask_select_kernel, kMsThreads, 0) !=
+                cudaSuccess || bps <= 0)
+            return cudaErrorInvalidConfiguration;
+        if (dev < 64) blocks_per_sm[dev] = bps;
+    }
+    const int64_t tiles = (p.T * p.Eu + kMsTile - 1) / kMsTile;
+    int64_t grid = (int64_t)device_sm_count() * bps;
+    if (grid > tiles) grid = tiles;
+    if (grid < 1) grid = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(kMsThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mask_select_kernel, map, p.T, p.Eu, p.n, probs, p.pes, tile_cnt, pp);
+}
+
 }  // namespace mr
 
 using namespace mr;
@@ -663,63 +694,35 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
 
     // ---- permuteProbs (maskedSelect or the padded lookup) --------------------
     auto launch_probs = [&](cudaStream_t ss) -> cudaError_t {
-        const int64_t ms_tiles = (p.T * p.Eu + kMsTile - 1) / kMsTile;
-        if (p.probs && !p.padded && !smap.map && ms_tiles <= kMsMaxTiles) {
-            static int ms_bps[64] = {0};
-            int dev = 0;
-            cudaGetDevice(&dev);
-            int bps = dev < 64 ? ms_bps[dev] : 0;
-            if (bps == 0) {
-                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, mask_select_kernel, kMsThreads, 0) !=
-                        cudaSuccess || bps <= 0)
-                    return cudaErrorInvalidConfiguration;
-                if (dev < 64) ms_bps[dev] = bps;
-            }
-            int64_t grid = (int64_t)device_sm_count() * bps;
-            if (grid > ms_tiles) grid = ms_tiles;
-            if (grid < 1) grid = 1;
-            cudaLaunchConfig_t cfg = {};
-            cfg.gridDim = dim3((unsigned)grid);
-            cfg.blockDim = dim3(kMsThreads);
-            cfg.dynamicSmemBytes = 0;
-            cfg.stream = ss;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeCooperative;
-            attr[0].val.cooperative = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            return cudaLaunchKernelEx(&cfg, mask_select_kernel, routingMap, p.T, p.Eu, p.n,
-                                      reinterpret_cast<const uint8_t*>(probs), p.pes,
-                                      reinterpret_cast<uint32_t*>(wp), pp);
-        }
-        if (p.probs && !p.padded && !smap.map) {
-            const int64_t nblk = (p.T + 31) / 32;
-            const int64_t items = nblk * p.Eu;
-            uint8_t* q = wp;
-            uint32_t* masks = reinterpret_cast<uint32_t*>(q);
-            q += align_up((uint64_t)items * 4u, 256);
-            uint32_t* offs = reinterpret_cast<uint32_t*>(q);
-            q += align_up((uint64_t)items * 4u, 256);
-            uint32_t* totals = reinterpret_cast<uint32_t*>(q);
-            q += align_up((uint64_t)p.Eu * 4u, 256);
-            uint32_t* bstart = reinterpret_cast<uint32_t*>(q);
-            q += align_up((uint64_t)(p.Eu + 1) * 4u, 256);
-            uint32_t* ticket = reinterpret_cast<uint32_t*>(q);
-            cudaError_t e = launch_pdl(mask_columns_kernel,
-                                       dim3(elementwise_grid(nblk * ((p.Eu + 31) / 32) * 32)),
-                                       dim3(256), 0, ss, routingMap, p.T, p.Eu, masks, offs, ticket);
-            if (e != cudaSuccess) return e;
-            GroupListOut none{nullptr, nullptr, 0};
-            e = csort_prefix(offs, nblk, (int)p.Eu, totals, bstart, ticket, none, ss);
-            if (e != cudaSuccess) return e;
-            const int64_t work = p.T * p.Eu > p.n ? p.T * p.Eu : p.n;
-            return launch_pdl(mask_scatter_kernel, dim3(elementwise_grid(work)), dim3(256), 0, ss,
-                              routingMap, (const uint32_t*)masks, (const uint32_t*)offs,
-                              (const uint32_t*)bstart, p.T, p.Eu, p.n,
-                              reinterpret_cast<const uint8_t*>(probs), p.pes, pp);
-        }
-        // padded with probs: the lookup runs in the sort's first scatter
-        return cudaSuccess;
+        // padded with probs: the lookup runs in the sort's first scatter; a
+        // small map: inside the gather-reduce
+        if (!p.probs || p.padded || smap.map) return cudaSuccess;
+        if ((p.T * p.Eu + kMsTile - 1) / kMsTile <= kMsMaxTiles)
+            return launch_mask_select(p, routingMap, reinterpret_cast<const uint8_t*>(probs),
+                                      reinterpret_cast<uint32_t*>(wp), pp, ss);
+        // beyond: column bitmasks, the prefix kernel, the scatter
+        const int64_t nblk = (p.T + 31) / 32;
+        const int64_t items = nblk * p.Eu;
+        uint8_t* q = wp;
+        uint32_t* masks = reinterpret_cast<uint32_t*>(q);
+        q += align_up((uint64_t)items * 4u, 256);
+        uint32_t* offs = reinterpret_cast<uint32_t*>(q);
+        q += align_up((uint64_t)items * 4u, 256);
+        uint32_t* totals = reinterpret_cast<uint32_t*>(q);
+        q += align_up((uint64_t)p.Eu * 4u, 256);
+        uint32_t* bstart = reinterpret_cast<uint32_t*>(q);
+        q += align_up((uint64_t)(p.Eu + 1) * 4u, 256);
+        uint32_t* ticket = reinterpret_cast<uint32_t*>(q);
+        cudaError_t e = launch_pdl(mask_columns_kernel, dim3(elementwise_grid(nblk * ((p.Eu + 31) / 32) * 32)),
+                                   dim3(256), 0, ss, routingMap, p.T, p.Eu, masks, offs, ticket);
+        if (e != cudaSuccess) return e;
+        GroupListOut none{nullptr, nullptr, 0};
+        e = csort_prefix(offs, nblk, (int)p.Eu, totals, bstart, ticket, none, ss);
+        if (e != cudaSuccess) return e;
+        const int64_t work = p.T * p.Eu > p.n ? p.T * p.Eu : p.n;
+        return launch_pdl(mask_scatter_kernel, dim3(elementwise_grid(work)), dim3(256), 0, ss, routingMap,
+                          (const uint32_t*)masks, (const uint32_t*)offs, (const uint32_t*)bstart, p.T, p.Eu,
+                          p.n, reinterpret_cast<const uint8_t*>(probs), p.pes, pp);
     };
 
     // ---- stable sort of sortedIndices -> outIndex, permuteTokenId ----------
