@@ -128,10 +128,21 @@ def sort_launches(n, key_range):
     return 3 * ((bits + 11) // 12)
 
 
+def masked_select_launches(T, Eu):
+    """Kernels of the not-padded maskedSelect, as the library plans it (vector
+    rows): none for a small map (T*Eu <= 16384, selected inside the reduce),
+    one cooperative kernel up to 4096 tiles of 1024 entries, else three."""
+    if T * Eu <= 16384:
+        return 0
+    return 1 if (T * Eu + 1023) // 1024 <= 4096 else 3
+
+
 def launches_per_step(spec):
     Y = spec["A"] * spec["BS"] * spec["K1"]
+    T = spec["A"] * spec["BS"]
     batching = 4  # rank, prefix, scatter, gather
-    unpermute = 3 + sort_launches(Y, Y + 1) + 1  # maskedSelect (3), index sort, reduce
+    # maskedSelect (the routing map is [T, topK+1]), index sort, reduce
+    unpermute = masked_select_launches(T, spec["K1"]) + sort_launches(Y, Y + 1) + 1
     return batching + unpermute
 
 

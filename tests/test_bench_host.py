@@ -40,16 +40,20 @@ def test_roundtrip_workload_bytes_are_about_six_gigabytes():
 
 def test_launch_count():
     spec = bench.workload_spec()
-    # batching: rank, prefix, scatter, gather; unpermute: maskedSelect (3),
-    # the index sort (147457 keys: a coarse pass of 3 launches and the fine
-    # sort), reduce
+    # batching: rank, prefix, scatter, gather; unpermute: maskedSelect (one
+    # cooperative kernel for the 16384 x 9 map), the index sort (147457 keys:
+    # a coarse pass of 3 launches and the fine sort), reduce
+    assert bench.masked_select_launches(64, 64) == 0
+    assert bench.masked_select_launches(16384, 9) == 1
+    assert bench.masked_select_launches(65536, 64) == 1
+    assert bench.masked_select_launches(65600, 64) == 3
     assert bench.sort_launches(147456, 147457) == 4
     assert bench.sort_launches(3000, 4096) == 3
     assert bench.sort_launches(512, 4096) == 1
     assert bench.sort_launches(4096, 4097) == 4
     assert bench.sort_launches(1 << 22, (1 << 22) + 1) == 6       # 23 bits: two LSD passes
     assert bench.sort_launches(1 << 24, (1 << 24) + 1) == 9       # 25 bits: three
-    assert bench.launches_per_step(spec) == 4 + 3 + 4 + 1
+    assert bench.launches_per_step(spec) == 4 + 1 + 4 + 1
 
 
 def test_contributing_rows_counts_valid_nonzero_slots():
