@@ -32,8 +32,10 @@
  *  - Outputs must not alias inputs or each other.
  *  - Results are deterministic: identical inputs give identical bits.
  *  - Execute calls can be captured into a CUDA graph (stream capture): they
- *    only enqueue kernels, memsets and event records/waits on `stream` and
- *    the auxiliary stream, which joins back. Make one call of each kind
+ *    only enqueue kernels (the not-padded moe_unpermute's maskedSelect is a
+ *    cooperative launch, whose grid never exceeds the blocks the device can
+ *    hold at once), memsets and event records/waits on `stream` and the
+ *    auxiliary stream, which joins back. Make one call of each kind
  *    outside any capture first (it creates the auxiliary stream and caches
  *    device queries), and capture ffnwb_batching_noalloc only after its
  *    first call on the device.
