@@ -1,0 +1,70 @@
+"""Repeated unpermute calls on two streams at once: every result must equal
+the first one bit for bit, and the first one the oracle. Covers each form of
+the weights' maskedSelect (inside the gather-reduce, the cooperative kernel,
+the three-kernel chain), the padded path and the no-probs path, with the
+index sort forked onto the library's auxiliary stream by both streams."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as w
+
+pytestmark = pytest.mark.gpu
+
+if not torch.cuda.is_available():
+    pytest.skip("needs a CUDA GPU", allow_module_level=True)
+
+import unpermute_stable_counting_gb300 as usc  # noqa: E402
+
+from _gpu_util import assert_unpermute_equal, float_tensor, to_dev, unpermute_numpy  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+CASES = {
+    "small_map": lambda: w.make_unpermute_topk(T=64, k=8, Eu=64, H=512, dtype=1, probs_dtype=1, seed=7),
+    "one_kernel_select": lambda: w.make_unpermute_topk(T=3000, k=6, Eu=48, H=256, dtype=1, probs_dtype=3,
+                                                       choices=(2, 6), seed=39),
+    "select_chain": lambda: w.make_unpermute_topk(T=65600, k=2, Eu=64, H=8, dtype=1, probs_dtype=3,
+                                                  choices=(1, 2), seed=41),
+    "padded_slack": lambda: w.make_unpermute_padded(T=2048, Eu=32, k=2, H=64, dtype=0, probs_dtype=3,
+                                                    mult=5, capacity=256, seed=42),
+    "no_probs": lambda: w.make_unpermute_topk(T=300, k=8, Eu=32, H=200, dtype=1, probs_dtype=None,
+                                              choices=(3, 8), seed=5),
+}
+
+
+@pytest.mark.parametrize("case", list(CASES))
+def test_repeated_calls_on_two_streams(case):
+    inp = CASES[case]()
+    ref = oracle.unpermute(inp)
+    probs = inp.get("probs")
+    dt, pdt = inp["tokenDtype"], inp["probsDtype"]
+    perm = float_tensor(inp["permuted"], dt)
+    si = to_dev(inp["sortedIndices"])
+    rm = to_dev(inp["routingMap"]) if probs is not None else None
+    pr = float_tensor(probs, pdt) if probs is not None else None
+    rs = None if probs is not None else (inp["T"], inp["H"])
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    outs = [None, None]
+    first = None
+    for it in range(60):
+        for j, st in enumerate(streams):
+            with torch.cuda.stream(st):
+                outs[j] = usc.moe_unpermute(perm, si, rm, pr, padded_mode=bool(inp["padded"]), restore_shape=rs,
+                                            out=outs[j])
+        if it % 10 == 9:
+            torch.cuda.synchronize()
+            for j in range(2):
+                got = unpermute_numpy(outs[j], inp)
+                if first is None:
+                    assert_unpermute_equal(got, ref, inp)
+                    first = got
+                for k, v in got.items():
+                    if v is not None:
+                        assert np.array_equal(v.view(np.uint8), first[k].view(np.uint8)), (it, j, k)
