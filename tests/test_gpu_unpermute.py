@@ -110,11 +110,13 @@ def test_topk_512_and_empty_tokens():
     check(inp)
 
 
-def test_more_routing_ones_than_slots():
-    """maskedSelect output longer than n: truncated."""
-    inp = w.make_unpermute_topk(T=40, k=4, Eu=10, H=16, dtype=3, probs_dtype=3, choices=(4,), seed=3)
+@pytest.mark.parametrize("T,Eu", [(40, 10), (2000, 16), (70000, 64)])
+def test_more_routing_ones_than_slots(T, Eu):
+    """maskedSelect output longer than n: truncated. The map sizes take the
+    small-map path, the one-kernel maskedSelect and the three-kernel one."""
+    inp = w.make_unpermute_topk(T=T, k=4, Eu=Eu, H=16, dtype=3, probs_dtype=3, choices=(4,), seed=3)
     inp["routingMap"][:] = 1
-    inp["probs"] = np.random.default_rng(3).random((40, 10)).astype(np.float32)
+    inp["probs"] = np.random.default_rng(3).random((T, Eu)).astype(np.float32)
     check(inp)
 
 
