@@ -21,12 +21,14 @@
 //   padded, probs     : permuteProbs[i] = probs[sortedIndices[i], i // capacity],
 //                       written by the sort's first scatter
 //   not padded        : the sort runs on the library's auxiliary stream,
-//                       overlapping the gather-reduce (fork/join events)
-//   always            : gather-reduce (reduce.cuh), one warp per (token,
-//                       hidden chunk), fp32 accumulation in ascending slot /
-//                       row order, atomic-free, one RNE cast per output
-//                       element; launched in plain stream order when short
-//                       and the sort runs beside it.
+//                       overlapping the maskedSelect and the gather-reduce
+//                       (fork/join events)
+//   always            : gather-reduce (reduce.cuh), one warp per (token, run
+//                       of hidden chunks), fp32 accumulation in ascending slot
+//                       / row order, atomic-free, one RNE cast per output
+//                       element; a persistent grid, or, when short and the
+//                       sort runs beside it, a plain-order launch of one work
+//                       unit per warp.
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
