@@ -69,6 +69,8 @@ FUZZ = [
     (16, 64, 64, 4096, 16, 1, 16, "zipf", 0.05),       # 65536 slots, 32 tiles
     (1024, 4, 8, 512, 8, 1, 1, "zipf", 0.1),           # A at its maximum (1024)
     (1024, 64, 32, 8192, 8, 1, 8, "zipf", 0.05),       # 2.1M slots (1024 tiles), 8192 experts
+    (2, 4, 5, 16, 65536, 1, 1, "zipf", 0.1),           # 128 KB rows
+    (2, 4, 5, 16, 65536, 2, 1, "zipf", 0.1),           # 64 KB int8 rows + scale (stride 65540)
 ]
 
 

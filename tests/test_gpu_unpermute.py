@@ -110,6 +110,16 @@ def test_topk_512_and_empty_tokens():
     check(inp)
 
 
+@pytest.mark.parametrize("padded", [0, 1])
+def test_wide_rows(padded):
+    """65536-element rows (512 hidden chunks of 64 vectors per token)."""
+    if padded:
+        inp = w.make_unpermute_padded(T=64, Eu=16, k=2, H=65536, dtype=1, probs_dtype=3, mult=3, seed=43)
+    else:
+        inp = w.make_unpermute_topk(T=24, k=4, Eu=12, H=65536, dtype=1, probs_dtype=1, choices=(2, 4), seed=44)
+    check(inp)
+
+
 @pytest.mark.parametrize("T,Eu", [(40, 10), (2000, 16), (70000, 64)])
 def test_more_routing_ones_than_slots(T, Eu):
     """maskedSelect output longer than n: truncated. The map sizes take the
