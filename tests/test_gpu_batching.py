@@ -71,6 +71,11 @@ FUZZ = [
     (1024, 64, 32, 8192, 8, 1, 8, "zipf", 0.05),       # 2.1M slots (1024 tiles), 8192 experts
     (2, 4, 5, 16, 65536, 1, 1, "zipf", 0.1),           # 128 KB rows
     (2, 4, 5, 16, 65536, 2, 1, "zipf", 0.1),           # 64 KB int8 rows + scale (stride 65540)
+    (3, 683, 1, 16, 24, 1, 1, "zipf", 0.1),            # 2049 slots: one-launch sort, 5 tiles, ragged
+    (8, 64, 9, 4097, 8, 2, 1, "uniform", 0.2),         # 4608 slots, 4098 keys: one-launch sort's key limit
+    (64, 64, 8, 4096, 8, 1, 1, "zipf", 0.05),          # 32768 slots: one-launch sort at 64 tiles
+    (3, 10923, 1, 4097, 8, 0, 1, "uniform", 0.1),      # 32769 slots: past it, the kernel chain
+    (4, 64, 9, 8192, 8, 1, 1, "zipf", 0.1),            # 2304 slots, 8193 keys: chain (key limit)
 ]
 
 

@@ -73,6 +73,8 @@ extern "C" mr_status ffnwb_batching_ex(const int32_t* expertIds, int32_t layerId
     uint8_t* wp = reinterpret_cast<uint8_t*>(workspace);
     CsortBufs cs = csort_carve(wp, p.Y, p.B);
     int32_t* gather_idx = reinterpret_cast<int32_t*>(wp);
+    wp += align_up((uint64_t)p.Y * 4u, 256);
+    if (csort_coop_bytes(p.Y, p.B) > 0) cs.coop_counts = reinterpret_cast<uint32_t*>(wp);
 
     BatchKey kf{expertIds, (int32_t)(layerId * p.El), (int32_t)p.El, (int32_t)p.E};
     GroupListOut gl{groupList, actualTokenNum, (int)p.E};

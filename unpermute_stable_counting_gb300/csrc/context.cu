@@ -138,7 +138,7 @@ static mr_status plan_context(int64_t expertNum, const int64_t* maxOutShape, int
     if (st != MR_OK) return st;
     p->B = (int)p->E + 2;  // experts, the masked sentinel E, and E + 1 for rows with no slot
     p->ws_bytes = csort_workspace_bytes(p->Y, p->B) + align_up((uint64_t)p->Y * 4u, 256);
-    *ws = p->ws_bytes + 3 * align_up((uint64_t)p->Y * 4u, 256);
+    *ws = p->ws_bytes + 3 * align_up((uint64_t)p->Y * 4u, 256) + csort_coop_bytes(p->Y, p->B);
     return MR_OK;
 }
 
@@ -194,6 +194,8 @@ extern "C" mr_status ffnwb_batching_context_ex(
     int32_t* sess = reinterpret_cast<int32_t*>(wp);
     wp += align_up((uint64_t)p.Y * 4u, 256);
     int32_t* micro = reinterpret_cast<int32_t*>(wp);
+    wp += align_up((uint64_t)p.Y * 4u, 256);
+    if (csort_coop_bytes(p.Y, p.B) > 0) cs.coop_counts = reinterpret_cast<uint32_t*>(wp);
 
     const uint8_t* ctx = reinterpret_cast<const uint8_t*>(scheduleContext);
     const int64_t row_stride = p.row_bytes + (int8 ? 4 : 0);

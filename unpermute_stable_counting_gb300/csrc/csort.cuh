@@ -56,6 +56,7 @@ struct CsortBufs {
     uint32_t* bucket_start;  // [B + 1]
     uint16_t* tile_rank;     // [N]
     uint32_t* ticket;        // [1]
+    uint32_t* coop_counts;   // key-major counts of the one-launch form (csort_coop.cuh), or null
 };
 
 inline uint64_t csort_workspace_bytes(int64_t N, int B) {
@@ -77,6 +78,7 @@ inline CsortBufs csort_carve(uint8_t*& p, int64_t N, int B) {
     p += align_up((uint64_t)N * 2u, 256);
     b.ticket = reinterpret_cast<uint32_t*>(p);
     p += 256;
+    b.coop_counts = nullptr;
     return b;
 }
 
