@@ -171,6 +171,17 @@ SORT_CASES = {
     # padded keys beyond 2^22: LSD passes and the CSR kernel
     "passes_padded_4m": lambda: w.make_unpermute_padded(T=1 << 22, Eu=16, k=1, H=4, dtype=0,
                                                         probs_dtype=3, mult=5, seed=19),
+    # two levels beside a small routing map (the gather-reduce selects the
+    # weights), without probs, with a map of 9 experts, and over 128 and 129
+    # tiles of 2048 entries
+    "two_level_small_map": lambda: w.make_unpermute_topk(T=512, k=10, Eu=32, H=16, dtype=1, probs_dtype=1,
+                                                         choices=(3, 10), seed=26),
+    "two_level_no_probs": lambda: permutation_case(100000, seed=27),
+    "two_level_nine_experts": lambda: w.make_unpermute_topk(T=4096, k=9, Eu=9, H=16, dtype=1, probs_dtype=1,
+                                                            choices=(7, 9), seed=28),
+    "two_level_128_tiles": lambda: w.make_unpermute_topk(T=32768, k=8, Eu=16, H=8, dtype=1, probs_dtype=3,
+                                                         choices=(5, 8), seed=29),
+    "two_level_129_tiles": lambda: permutation_case(262145, seed=30),
     # 32800 tokens x 512 slots: 16.8M rows, 25-bit keys (topK_num at its maximum)
     "three_passes": lambda: w.make_unpermute_topk(T=32800, k=512, Eu=16, H=8, dtype=1, probs_dtype=1,
                                                   choices=(1, 2), seed=17),

@@ -128,7 +128,7 @@ __device__ __forceinline__ float load_f32(const void* base, int64_t i, int dt) {
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-inline uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
+__host__ __device__ inline uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }
 
 int device_sm_count();                 // cached per device
 

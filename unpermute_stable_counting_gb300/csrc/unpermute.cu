@@ -35,25 +35,12 @@
 
 #include <cooperative_groups.h>
 
+#include "index_sort.cuh"
 #include "reduce.cuh"
 #include "routing.cuh"
 
 namespace mr {
 namespace cg = cooperative_groups;
-
-// Copy one element of 2 or 4 bytes (the probs dtype) without interpreting it.
-__device__ __forceinline__ void copy_prob(uint8_t* dst, int64_t di, const uint8_t* src, int64_t si,
-                                          int pes) {
-    if (pes == 4) {
-        reinterpret_cast<uint32_t*>(dst)[di] = __ldg(reinterpret_cast<const uint32_t*>(src) + si);
-    } else {
-        reinterpret_cast<uint16_t*>(dst)[di] = __ldg(reinterpret_cast<const unsigned short*>(src) + si);
-    }
-}
-__device__ __forceinline__ void zero_prob(uint8_t* dst, int64_t di, int pes) {
-    if (pes == 4) reinterpret_cast<uint32_t*>(dst)[di] = 0u;
-    else reinterpret_cast<uint16_t*>(dst)[di] = 0;
-}
 
 // One thread per (token, expert) element: a routed element lands at
 // bucket_start[e] + offs[blk][e] + (routed tokens of its block below it).
@@ -92,6 +79,15 @@ constexpr int kMsPer = 4;
 constexpr int64_t kMsTile = (int64_t)kMsThreads * kMsPer;
 constexpr int64_t kMsMaxTiles = 4096;
 
+__device__ __forceinline__ uint32_t ld_prob_bits(const uint8_t* p, int64_t i, int pes) {
+    return pes == 4 ? __ldg(reinterpret_cast<const uint32_t*>(p) + i)
+                    : (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p) + i);
+}
+__device__ __forceinline__ void st_prob_bits(uint8_t* p, int64_t i, uint32_t v, int pes) {
+    if (pes == 4) reinterpret_cast<uint32_t*>(p)[i] = v;
+    else reinterpret_cast<uint16_t*>(p)[i] = (uint16_t)v;
+}
+
 __global__ void __launch_bounds__(kMsThreads)
 mask_select_kernel(const int8_t* __restrict__ map, int64_t T, int64_t Eu, int64_t n,
                    const uint8_t* __restrict__ probs, int pes, uint32_t* __restrict__ tile_cnt,
@@ -101,6 +97,56 @@ mask_select_kernel(const int8_t* __restrict__ map, int64_t T, int64_t Eu, int64_
     pdl_enter();  // launched in plain stream order (cooperative): returns at once
     const int64_t N = T * Eu;
     const int64_t ntiles = (N + kMsTile - 1) / kMsTile;
+    if (ntiles <= (int64_t)gridDim.x) {
+        // One tile per block: the map entries, their probs (loaded together
+        // with the map, whether routed or not) and the in-tile positions stay
+        // in registers across the grid barrier; after it only the tile's base
+        // position is added and the probs are stored.
+        const int64_t tile = blockIdx.x;
+        const bool has = tile < ntiles;
+        const int64_t f0 = tile * kMsTile + (int64_t)threadIdx.x * kMsPer;
+        int64_t e = f0 / T, t = f0 - e * T;
+        int8_t m[kMsPer];
+        uint32_t pv[kMsPer];
+#pragma unroll
+        for (int q = 0; q < kMsPer; ++q) {
+            const bool in = has && f0 + q < N;
+            m[q] = in ? map[t * Eu + e] : (int8_t)0;
+            pv[q] = in ? ld_prob_bits(probs, t * Eu + e, pes) : 0u;
+            if (++t == T) {
+                t = 0;
+                ++e;
+            }
+        }
+        uint32_t c = 0u;
+#pragma unroll
+        for (int q = 0; q < kMsPer; ++q) c += m[q] != 0 ? 1u : 0u;
+        uint32_t tot = 0u;
+        const uint32_t excl = block_exclusive_scan(c, wsum, &tot);
+        if (has && threadIdx.x == 0) tile_cnt[tile] = tot;
+        grid.sync();
+        uint32_t s_lo = 0u, s_all = 0u;
+        for (int64_t u = threadIdx.x; u < ntiles; u += kMsThreads) {
+            const uint32_t v = __ldcg(&tile_cnt[u]);
+            s_all += v;
+            if (u < tile) s_lo += v;
+        }
+        uint32_t below = 0u, nnz = 0u;
+        block_exclusive_scan(s_lo, wsum, &below);
+        block_exclusive_scan(s_all, wsum, &nnz);
+        uint32_t pos = below + excl;
+#pragma unroll
+        for (int q = 0; q < kMsPer; ++q) {
+            if (m[q] != 0) {
+                if ((int64_t)pos < n) st_prob_bits(pp, pos, pv[q], pes);
+                ++pos;
+            }
+        }
+        const int64_t stride = (int64_t)gridDim.x * kMsThreads;
+        for (int64_t i = (int64_t)nnz + (int64_t)blockIdx.x * kMsThreads + threadIdx.x; i < n; i += stride)
+            zero_prob(pp, i, pes);
+        return;
+    }
     for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
         const int64_t f0 = tile * kMsTile + (int64_t)threadIdx.x * kMsPer;
         int64_t e = f0 / T, t = f0 - e * T;
@@ -161,208 +207,12 @@ mask_select_kernel(const int8_t* __restrict__ map, int64_t T, int64_t Eu, int64_
 }
 
 // ---------------------------------------------------------------------------
-// Stable sort of sortedIndices (LSD passes of the counting-sort engine, or a
-// coarse pass followed by one block per coarse bucket).
-// Full key: not padded (invalid first) v+1 for 0 <= v < rows, else 0;
-//           padded (invalid last)      v   for 0 <= v < T,    else T.
-// The coarse digit of the two-level sort keeps the invalid entries alone in a
-// bucket of their own, so that their final places are known after the coarse
-// pass: not padded, bucket 0 (1 + (key - 1) >> shift for the others); padded,
-// the last bucket (key >> shift for the others).
-// ---------------------------------------------------------------------------
-struct RadixKey {
-    const int32_t* si;        // pass 0 source
-    const uint32_t* keys_in;  // later passes: full keys in the previous order
-    int64_t limit;            // rows (not padded) or T (padded)
-    int padded;
-    int shift;
-    uint32_t mask;
-    int coarse_invalid_apart;  // two levels: digit as described above
-    uint32_t invalid_bucket;   // padded, two levels: the last coarse bucket
-    __device__ __forceinline__ uint32_t full(int64_t i) const {
-        if (keys_in) return keys_in[i];
-        const int32_t v = si[i];
-        const bool ok = v >= 0 && (int64_t)v < limit;
-        if (padded) return ok ? (uint32_t)v : (uint32_t)limit;
-        return ok ? (uint32_t)v + 1u : 0u;
-    }
-    __device__ __forceinline__ int digit(uint32_t fk) const {
-        if (coarse_invalid_apart) {
-            if (padded) return fk == (uint32_t)limit ? (int)invalid_bucket : (int)(fk >> shift);
-            return fk == 0u ? 0 : (int)(1u + ((fk - 1u) >> shift));
-        }
-        return (int)((fk >> shift) & mask);
-    }
-    __device__ __forceinline__ int operator()(int64_t i) const { return digit(full(i)); }
-};
-
-// The padded probs lookup of the first pass (pp != nullptr): it reads the same
-// sortedIndices element as the key.
-struct PaddedProbs {
-    const uint8_t* probs;
-    uint8_t* pp;
-    int64_t Eu, cap;
-    int pes;
-};
-
-// The scatter step of one sort pass for item i at position d: the full key
-// and the item's original index move to d (every pass but the last); the last
-// pass writes outIndex and permuteTokenId instead. The first pass of a padded
-// sort with probs also writes permuteProbs[i]. In the coarse pass of the
-// two-level sort an invalid entry is already in its final place (its bucket,
-// first when not padded and last when padded, keeps the original order): it
-// writes outIndex and permuteTokenId at once (final_index, final_ptid).
-struct RadixScatter {
-    RadixKey kf;
-    const int32_t* idx_in;
-    uint32_t* keys_out;
-    int32_t* idx_out;
-    int32_t* out_index;
-    int32_t* ptid;
-    int64_t topk;
-    PaddedProbs pprobs;
-    int32_t* final_index;
-    int32_t* final_ptid;
-    __device__ __forceinline__ void operator()(int64_t i, int, uint32_t d, uint32_t) const {
-        if (pprobs.pp) {
-            // permuteProbs[i] = probs[sortedIndices[i], i // capacity], 0 if invalid
-            const int32_t v = kf.si[i];
-            if (v >= 0 && (int64_t)v < kf.limit) {
-                copy_prob(pprobs.pp, i, pprobs.probs, (int64_t)v * pprobs.Eu + i / pprobs.cap, pprobs.pes);
-            } else {
-                zero_prob(pprobs.pp, i, pprobs.pes);
-            }
-        }
-        const uint32_t fk = kf.full(i);
-        const int32_t idx = idx_in ? idx_in[i] : (int32_t)i;
-        if (final_index && fk == (kf.padded ? (uint32_t)kf.limit : 0u)) {
-            final_index[d] = idx;
-            final_ptid[d] = kf.padded ? kf.si[idx] : (int32_t)(idx / topk);
-            return;
-        }
-        keys_out[d] = fk;
-        if (out_index) {
-            out_index[d] = idx;
-            ptid[d] = kf.padded ? kf.si[idx] : (int32_t)(idx / topk);
-        } else {
-            idx_out[d] = idx;
-        }
-    }
-};
-
-__global__ void __launch_bounds__(256)
-radix_scatter_kernel(RadixKey kf, int64_t n, int B, CsortBufs cs, RadixScatter sc) {
-    pdl_enter();
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-        const int digit = kf(i);
-        sc(i, digit, csort_dest(digit, i, cs, B), 0u);
-    }
-}
-
-// Second level of the two-level sort (one block per coarse bucket). The first
-// level is a counting-sort pass on the coarse digit, which leaves each coarse
-// bucket [cstart[c], cstart[c+1]) in original order. The block sorts its
-// bucket stably by the low s bits of its key (F = 2^s fine keys): a histogram
-// and its scan give the fine starts, and 256-item chunks taken in order are
-// ranked by key with warp matches, per-warp counters and a running count per
-// fine key.
-//   padded:     digit key >> s, fine key = key & (F-1); the fine starts are
-//               the CSR row pointers ptr[c*F + f] (the last block also writes
-//               ptr[T], the start of the invalid bucket that follows it);
-//               permuteTokenId = the value.
-//   not padded: block b sorts bucket b+1 by (key - 1) & (F-1);
-//               permuteTokenId = original index / topK.
-// The coarse pass has placed the invalid entries' bucket, which no block takes.
-constexpr int kFineThreads = 256;
-constexpr int kFineWarps = kFineThreads / 32;
-constexpr int kMaxFineBits = 10;
-
-template <bool PADDED>
-__global__ void __launch_bounds__(kFineThreads)
-fine_sort_kernel(const uint32_t* __restrict__ keys, const int32_t* __restrict__ idx,
-                 const uint32_t* __restrict__ cstart, int shift, int64_t T, int64_t topk,
-                 const int32_t* __restrict__ si, int32_t* __restrict__ out_index,
-                 int32_t* __restrict__ ptid, int32_t* __restrict__ ptr) {
-    extern __shared__ __align__(16) uint32_t fsm[];
-    const int F = 1 << shift;
-    uint32_t* hist = fsm;                     // [F] counts, then fine starts
-    uint32_t* running = fsm + F;              // [F] items placed so far
-    uint32_t* wcnt = fsm + 2 * F;             // [kFineWarps][F] this chunk's counts
-    pdl_enter();
-    const int c = PADDED ? (int)blockIdx.x : (int)blockIdx.x + 1;
-    const uint32_t lo = cstart[c], hi = cstart[c + 1];
-    const int warp = threadIdx.x >> 5;
-    const uint32_t fmask = (uint32_t)F - 1u;
-    const uint32_t kofs = PADDED ? 0u : 1u;
-    for (int i = threadIdx.x; i < (2 + kFineWarps) * F; i += kFineThreads) fsm[i] = 0u;
-    __syncthreads();
-    for (uint32_t i = lo + threadIdx.x; i < hi; i += kFineThreads)
-        atomicAdd(&hist[(keys[i] - kofs) & fmask], 1u);
-    __syncthreads();
-    if (threadIdx.x == 0) {  // F <= 1024 counts: a serial scan is a few hundred cycles
-        uint32_t run = 0u;
-        for (int f = 0; f < F; ++f) {
-            const uint32_t h = hist[f];
-            hist[f] = run;
-            run += h;
-        }
-    }
-    __syncthreads();
-    if (PADDED) {  // row pointers of the tokens in this coarse bucket
-        for (int f = threadIdx.x; f < F; f += kFineThreads) {
-            const int64_t t = (int64_t)c * F + f;
-            if (t < T) ptr[t] = (int32_t)(lo + hist[f]);
-        }
-        if (c == (int)gridDim.x - 1 && threadIdx.x == 0) ptr[T] = (int32_t)hi;
-    }
-    const uint32_t lt = lanemask_lt();
-    for (uint32_t base = lo; base < hi; base += kFineThreads) {
-        const uint32_t i = base + threadIdx.x;
-        const bool in = i < hi;
-        const int f = in ? (int)((keys[i] - kofs) & fmask) : -1;
-        const uint32_t peers = __match_any_sync(0xffffffffu, f);
-        const uint32_t below = __popc(peers & lt);
-        const bool leader = in && below == 0u;
-        if (leader) wcnt[warp * F + f] = __popc(peers);
-        __syncthreads();
-        if (in) {
-            uint32_t r = below + running[f] + hist[f];
-            for (int w = 0; w < warp; ++w) r += wcnt[w * F + f];
-            const uint32_t pos = lo + r;
-            const int32_t o = idx[i];
-            out_index[pos] = o;
-            ptid[pos] = PADDED ? si[o] : (int32_t)(o / topk);
-        }
-        __syncthreads();
-        if (leader) {
-            atomicAdd(&running[f], (uint32_t)__popc(peers));
-            wcnt[warp * F + f] = 0u;
-        }
-        __syncthreads();
-    }
-}
-
-// ptr[t] = first position of the sorted keys with key >= t, t in [0, T].
-__global__ void __launch_bounds__(256)
-csr_from_keys_kernel(const uint32_t* __restrict__ keys, int64_t n, int64_t T,
-                     int32_t* __restrict__ ptr) {
-    pdl_enter();
-    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    for (int64_t p = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; p <= n; p += stride) {
-        const int64_t prev = p > 0 ? (int64_t)keys[p - 1] : -1;
-        const int64_t cur = p < n ? (int64_t)keys[p] : T + 1;
-        const int64_t hi = cur < T ? cur : T;
-        for (int64_t t = prev + 1; t <= hi; ++t) ptr[t] = (int32_t)p;
-    }
-}
-
-// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 
 constexpr int kRadixDigitBits = 12;
 constexpr double kPdlReduceBytes = 1e9;  // see the not-padded launch below
+constexpr int64_t kSortReserveSMs = 8;    // SMs a short reduce leaves to the concurrent sort
 
 struct UnpermutePlan {
     int64_t rows, H, n, T, Eu, topk, cap;
@@ -563,14 +413,19 @@ static cudaError_t launch_reduce_vec(const UnpermutePlan& p, const uint8_t* perm
                                      : unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED, kRedRun, SMALL>;
     if (!pdl) {
         // A short reduce launched in plain order has the index sort running
-        // beside it on the (higher-priority) auxiliary stream: one work unit
-        // per warp, so that blocks retire as they finish and the sort's blocks
-        // take the freed slots, instead of a persistent grid that holds every
-        // SM until its end (measured on GB300: top-k T=4096, k=8, H=4096
-        // 55.6 -> 53.5 us; the reduce itself 41 -> 43 us)
+        // beside it on the (higher-priority) auxiliary stream. Its grid is one
+        // work unit per warp (blocks retire as they finish and the sort's
+        // blocks take the freed slots), capped at a persistent grid on all
+        // SMs but kSortReserveSMs, so that the sort also has SMs of its own
+        // (measured on GB300, top-k T=4096, k=8, H=4096: a persistent grid on
+        // every SM 55.6 us, one unit per warp 53.5 us, with the cap 51.5 us;
+        // a decode step's few units stay below the cap)
         const int64_t run = long_units < cap * 8 ? 1 : kRedRun;
         const int64_t units = p.T * ((chunks + run - 1) / run);
         grid = (units + 7) / 8;
+        const int64_t sms = device_sm_count();
+        const int64_t pgrid = (sms > 2 * kSortReserveSMs ? sms - kSortReserveSMs : sms) * bps;
+        if (grid > pgrid) grid = pgrid;
         if (grid > 0x7fffffff) grid = 0x7fffffff;
         if (grid < 1) grid = 1;
     }
@@ -694,39 +549,6 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
     if (use_small_map(p, permutedTokens, unpermutedTokens))
         smap = SmallMap{routingMap, reinterpret_cast<const uint8_t*>(probs), pp, p.Eu};
 
-    // ---- permuteProbs (maskedSelect or the padded lookup) --------------------
-    auto launch_probs = [&](cudaStream_t ss) -> cudaError_t {
-        // padded with probs: the lookup runs in the sort's first scatter; a
-        // small map: inside the gather-reduce
-        if (!p.probs || p.padded || smap.map) return cudaSuccess;
-        if ((p.T * p.Eu + kMsTile - 1) / kMsTile <= kMsMaxTiles)
-            return launch_mask_select(p, routingMap, reinterpret_cast<const uint8_t*>(probs),
-                                      reinterpret_cast<uint32_t*>(wp), pp, ss);
-        // beyond: column bitmasks, the prefix kernel, the scatter
-        const int64_t nblk = (p.T + 31) / 32;
-        const int64_t items = nblk * p.Eu;
-        uint8_t* q = wp;
-        uint32_t* masks = reinterpret_cast<uint32_t*>(q);
-        q += align_up((uint64_t)items * 4u, 256);
-        uint32_t* offs = reinterpret_cast<uint32_t*>(q);
-        q += align_up((uint64_t)items * 4u, 256);
-        uint32_t* totals = reinterpret_cast<uint32_t*>(q);
-        q += align_up((uint64_t)p.Eu * 4u, 256);
-        uint32_t* bstart = reinterpret_cast<uint32_t*>(q);
-        q += align_up((uint64_t)(p.Eu + 1) * 4u, 256);
-        uint32_t* ticket = reinterpret_cast<uint32_t*>(q);
-        cudaError_t e = launch_pdl(mask_columns_kernel, dim3(elementwise_grid(nblk * ((p.Eu + 31) / 32) * 32)),
-                                   dim3(256), 0, ss, routingMap, p.T, p.Eu, masks, offs, ticket);
-        if (e != cudaSuccess) return e;
-        GroupListOut none{nullptr, nullptr, 0};
-        e = csort_prefix(offs, nblk, (int)p.Eu, totals, bstart, ticket, none, ss);
-        if (e != cudaSuccess) return e;
-        const int64_t work = p.T * p.Eu > p.n ? p.T * p.Eu : p.n;
-        return launch_pdl(mask_scatter_kernel, dim3(elementwise_grid(work)), dim3(256), 0, ss, routingMap,
-                          (const uint32_t*)masks, (const uint32_t*)offs, (const uint32_t*)bstart, p.T, p.Eu,
-                          p.n, reinterpret_cast<const uint8_t*>(probs), p.pes, pp);
-    };
-
     // ---- stable sort of sortedIndices -> outIndex, permuteTokenId ----------
     uint8_t* q = wp + p.ms_bytes;
     const int Bsort = p.fine_bits ? p.Bmax : p.passes == 1 ? (int)p.key_range : p.Bmax;
@@ -799,6 +621,39 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
                               ss, kin, p.n, p.T, ptr);
         }
         return cudaSuccess;
+    };
+
+    // ---- permuteProbs (maskedSelect or the padded lookup) --------------------
+    auto launch_probs = [&](cudaStream_t ss) -> cudaError_t {
+        // padded with probs: the lookup runs in the sort's first scatter; a
+        // small map: inside the gather-reduce
+        if (!p.probs || p.padded || smap.map) return cudaSuccess;
+        if ((p.T * p.Eu + kMsTile - 1) / kMsTile <= kMsMaxTiles)
+            return launch_mask_select(p, routingMap, reinterpret_cast<const uint8_t*>(probs),
+                                      reinterpret_cast<uint32_t*>(wp), pp, ss);
+        // beyond: column bitmasks, the prefix kernel, the scatter
+        const int64_t nblk = (p.T + 31) / 32;
+        const int64_t items = nblk * p.Eu;
+        uint8_t* q = wp;
+        uint32_t* masks = reinterpret_cast<uint32_t*>(q);
+        q += align_up((uint64_t)items * 4u, 256);
+        uint32_t* offs = reinterpret_cast<uint32_t*>(q);
+        q += align_up((uint64_t)items * 4u, 256);
+        uint32_t* totals = reinterpret_cast<uint32_t*>(q);
+        q += align_up((uint64_t)p.Eu * 4u, 256);
+        uint32_t* bstart = reinterpret_cast<uint32_t*>(q);
+        q += align_up((uint64_t)(p.Eu + 1) * 4u, 256);
+        uint32_t* ticket = reinterpret_cast<uint32_t*>(q);
+        cudaError_t e = launch_pdl(mask_columns_kernel, dim3(elementwise_grid(nblk * ((p.Eu + 31) / 32) * 32)),
+                                   dim3(256), 0, ss, routingMap, p.T, p.Eu, masks, offs, ticket);
+        if (e != cudaSuccess) return e;
+        GroupListOut none{nullptr, nullptr, 0};
+        e = csort_prefix(offs, nblk, (int)p.Eu, totals, bstart, ticket, none, ss);
+        if (e != cudaSuccess) return e;
+        const int64_t work = p.T * p.Eu > p.n ? p.T * p.Eu : p.n;
+        return launch_pdl(mask_scatter_kernel, dim3(elementwise_grid(work)), dim3(256), 0, ss, routingMap,
+                          (const uint32_t*)masks, (const uint32_t*)offs, (const uint32_t*)bstart, p.T, p.Eu,
+                          p.n, reinterpret_cast<const uint8_t*>(probs), p.pes, pp);
     };
 
     // ---- gather-reduce --------------------------------------------------------
