@@ -14,7 +14,10 @@ than L2 (2.1 GB of token rows per step), so no L2 flush is needed.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 --impl reference times the CPU oracle (the program the kernels are checked
-against) on the host cores, on a bounded sample of the same workload.
+against) on one host core: on the full workload when --warmup + --steps
+full-size steps fit about REFERENCE_BUDGET_S (a 20-step run does), else on
+a power-of-two fraction of its attention workers, which the line's
+config.sample names.
 """
 from __future__ import annotations
 
@@ -52,8 +55,10 @@ def parse_args(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--cpu-sample-attn", type=int, default=32,
-                    help="attention workers (A) of the oracle's bounded sample (full workload: 256)")
+    ap.add_argument("--cpu-sample-attn", type=int, default=None,
+                    help="attention workers (A) of each reference-arm step (default: the full "
+                         "workload's 256 when --steps + --warmup oracle steps fit "
+                         "REFERENCE_BUDGET_S, else the largest power-of-two fraction that does)")
     ap.add_argument("--small", action="store_true", help="a small case of the same workload (profiling)")
     ap.add_argument("--workload", choices=["roundtrip", "tiny", "topk", "int8", "padded", "context",
                                            "batching", "permute", "permute_padded", "update_expert", "decode_unpermute",
@@ -305,13 +310,31 @@ def cpu_baseline(spec, inp, rmap, probs, ab):
                        f"single-threaded oracle, input generation excluded")}
 
 
+REFERENCE_BUDGET_S = 150.0   # whole reference run: --warmup + --steps oracle steps
+ORACLE_STEP_S_FULL = 1.9     # one oracle step of the full workload on a GB300 machine's Grace core
+
+
+def reference_attn(args) -> int:
+    """Attention workers of each reference-arm step: the full workload (256)
+    when warmup + steps full-size oracle steps fit the budget, else the
+    largest power-of-two fraction of it that does (at least 8)."""
+    if args.cpu_sample_attn is not None:
+        return args.cpu_sample_attn
+    full = w.ROUNDTRIP_BATCHING["A"]
+    n = max(1, args.steps + args.warmup)
+    a = full
+    while a > 8 and n * ORACLE_STEP_S_FULL * a / full > REFERENCE_BUDGET_S:
+        a //= 2
+    return a
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     import oracle
     oracle.build()
-    spec = workload_spec(attn=args.cpu_sample_attn)
+    spec = workload_spec(attn=reference_attn(args))
     inp, rmap, probs, U = make_host_inputs(spec)
     V = contributing_rows(spec, inp, probs)
     ab = algorithmic_bytes(spec, U, V)
@@ -320,8 +343,14 @@ def run_reference(args):
     times = [oracle_step(spec, inp, rmap, probs) for _ in range(args.steps)]
     total = sum(times)
     value = ab["total"] * args.steps / total / 1e9
-    sample = (f"each step: the round trip with A={spec['A']} attention workers instead of 256 "
-              f"(Y={ab['slots']} slots, {ab['tokens']} tokens, H=7168) on the single-threaded CPU oracle")
+    full = w.ROUNDTRIP_BATCHING["A"]
+    if spec["A"] == full:
+        sample = (f"each step: the full workload (A={full}, Y={ab['slots']} slots, {ab['tokens']} tokens, "
+                  f"H=7168) on the single-threaded CPU oracle")
+    else:
+        sample = (f"A={spec['A']} of {full}: each step the round trip with {spec['A']} attention workers "
+                  f"(Y={ab['slots']} slots, {ab['tokens']} tokens, H=7168) on the single-threaded CPU "
+                  f"oracle, so that {args.warmup + args.steps} steps fit {REFERENCE_BUDGET_S:.0f} s")
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",

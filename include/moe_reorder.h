@@ -19,10 +19,18 @@
  *  - Pointers named as device pointers must point to device memory of the
  *    current CUDA device; pointers named host pointers to host memory.
  *  - The caller owns and frees every buffer, including the workspace. The
- *    library allocates no device memory and keeps no per-call state. The
- *    not-padded moe_unpermute keeps one auxiliary stream and two events per
- *    device (created on first use, kept until exit): its sort of
- *    sortedIndices runs there, forked from and joined back into `stream`.
+ *    library allocates no device memory and keeps no per-call state, with two
+ *    exceptions, both created on first use and kept until exit:
+ *    (1) the not-padded moe_unpermute keeps, per device and per caller
+ *    `stream` (up to 64 caller streams per device), one auxiliary stream and
+ *    two events: its sort of sortedIndices runs there, forked from and joined
+ *    back into `stream`. Calls on different caller streams never share an
+ *    auxiliary stream, so their sorts overlap and a stream capture on one
+ *    caller stream does not reach calls on another. Past 64 caller streams
+ *    on a device, the sort runs in `stream` itself.
+ *    (2) ffnwb_batching_noalloc's fixed scratch array (see there).
+ *    Both belong to the device's context: do not use the library across a
+ *    cudaDeviceReset.
  *  - Execute calls are asynchronous on `stream` (a cudaStream_t; NULL = the
  *    legacy default stream). Outputs are valid once the caller synchronises
  *    the stream. Nothing is read back to the host.
@@ -32,13 +40,14 @@
  *  - Outputs must not alias inputs or each other.
  *  - Results are deterministic: identical inputs give identical bits.
  *  - Execute calls can be captured into a CUDA graph (stream capture): they
- *    only enqueue kernels (the not-padded moe_unpermute's maskedSelect is a
- *    cooperative launch, whose grid never exceeds the blocks the device can
- *    hold at once), memsets and event records/waits on `stream` and the
- *    auxiliary stream, which joins back. Make one call of each kind
- *    outside any capture first (it creates the auxiliary stream and caches
- *    device queries), and capture ffnwb_batching_noalloc only after its
- *    first call on the device.
+ *    only enqueue kernels (the not-padded moe_unpermute's maskedSelect and
+ *    the batching's one-launch sort of up to 32768 slots are cooperative
+ *    launches, whose grids never exceed the blocks the device can hold at
+ *    once), memsets and event records/waits on `stream` and its auxiliary
+ *    stream, which joins back. Make one call of each kind on each caller
+ *    stream outside any capture first (it creates that stream's auxiliary
+ *    stream and caches device queries), and capture ffnwb_batching_noalloc
+ *    only after its first call on the device.
  */
 #ifndef MOE_REORDER_H
 #define MOE_REORDER_H
@@ -264,8 +273,12 @@ mr_status ffnwb_batching_context_ex(const void* scheduleContext, int64_t expertN
  *   cudaMalloc's implicit synchronisation. This entry point computes exactly
  *   what ffnwb_batching computes, with the same arguments minus the workspace,
  *   and allocates nothing: its scratch is a fixed array of
- *   MR_NOALLOC_SCRATCH_BYTES compiled into the library, which every GPU that
- *   loads the library holds until the process exits.
+ *   MR_NOALLOC_SCRATCH_BYTES compiled into the library, which a GPU holds
+ *   from the moment the library's code is loaded there until the process
+ *   exits. Under CUDA's default lazy module loading that is the first call
+ *   on the device, which may therefore allocate: make one call per device
+ *   during start-up (before reserving the device's memory), or set
+ *   CUDA_MODULE_LOADING=EAGER. Later calls allocate nothing.
  *   - Calls that need more scratch than the array holds return
  *     MR_ERR_WORKSPACE (4 MiB covers, e.g., Y = 147456 slots with
  *     expertNum = 8192, or Y = 262144 slots with expertNum = 1024).

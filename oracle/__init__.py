@@ -11,7 +11,9 @@ from __future__ import annotations
 
 import ctypes
 import fcntl
+import hashlib
 import os
+import platform
 import subprocess
 
 import numpy as np
@@ -19,6 +21,7 @@ import numpy as np
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.cpp")
 _LIB = os.path.join(_HERE, "liboracle.so")
+_CFLAGS = ["-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
 # A prebuilt oracle library to load instead (the mutation tests point this at a
 # copy of the oracle with a planted mistake).
 _LIB_OVERRIDE = os.environ.get("USC_ORACLE_LIB")
@@ -32,15 +35,28 @@ _I32 = ctypes.c_int32
 def compile_library(src: str, out: str) -> str:
     """Compile one oracle source file into a shared library."""
     tmp = out + f".tmp{os.getpid()}"
-    cmd = ["g++", "-O2", "-std=c++17", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
-           "-shared", "-o", tmp, src]
+    cmd = ["g++"] + _CFLAGS + ["-o", tmp, src]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
 
 
+def _digest() -> str:
+    """SHA-256 of the oracle source, the compile command and the machine type:
+    the library is rebuilt whenever its stamp differs (content, not times)."""
+    h = hashlib.sha256()
+    with open(_SRC, "rb") as f:
+        h.update(f.read())
+    h.update(" ".join(_CFLAGS).encode() + platform.machine().encode())
+    return h.hexdigest()
+
+
 def _stale() -> bool:
-    return not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+    stamp = _LIB + ".sha256"
+    if not os.path.exists(_LIB) or not os.path.exists(stamp):
+        return True
+    with open(stamp) as f:
+        return f.read().strip() != _digest()
 
 
 def build(force: bool = False) -> str:
@@ -51,6 +67,8 @@ def build(force: bool = False) -> str:
             try:
                 if force or _stale():
                     compile_library(_SRC, _LIB)
+                    with open(_LIB + ".sha256", "w") as f:
+                        f.write(_digest() + "\n")
             finally:
                 fcntl.flock(lk, fcntl.LOCK_UN)
     return _LIB

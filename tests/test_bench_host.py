@@ -119,3 +119,15 @@ def test_reference_arm_other_ranks_print_nothing():
                         "--warmup", "0", "--cpu-sample-attn", "2"], cwd=ROOT, capture_output=True,
                        text=True, timeout=600, env=env)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_reference_arm_size_follows_the_step_budget():
+    """The reference arm times the full workload (A = 256) when the run's
+    warmup + steps fit its time budget, else a power-of-two fraction."""
+    sys.path.insert(0, ROOT)
+    import bench
+    full = bench.reference_attn(bench.parse_args(["--impl", "reference", "--steps", "20", "--warmup", "3"]))
+    assert full == 256
+    part = bench.reference_attn(bench.parse_args(["--impl", "reference", "--steps", "200", "--warmup", "10"]))
+    assert part < 256 and 210 * bench.ORACLE_STEP_S_FULL * part / 256 <= bench.REFERENCE_BUDGET_S
+    assert bench.reference_attn(bench.parse_args(["--cpu-sample-attn", "2"])) == 2

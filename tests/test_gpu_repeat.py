@@ -68,3 +68,65 @@ def test_repeated_calls_on_two_streams(case):
                 for k, v in got.items():
                     if v is not None:
                         assert np.array_equal(v.view(np.uint8), first[k].view(np.uint8)), (it, j, k)
+
+
+def test_capture_on_one_stream_beside_eager_calls_on_another():
+    """A not-padded unpermute captured on stream A while an eager one runs on
+    stream B: each caller stream has its own auxiliary stream, so the eager
+    call's sort fork does not touch the capture (with one auxiliary stream
+    shared by both, the eager fork would record into a capturing stream).
+    The replayed graph and the eager call must both equal the oracle."""
+    a = w.make_unpermute_topk(T=512, k=8, Eu=64, H=256, dtype=1, probs_dtype=1, choices=(4, 8), seed=61)
+    b = w.make_unpermute_topk(T=700, k=6, Eu=32, H=128, dtype=1, probs_dtype=1, choices=(2, 6), seed=62)
+
+    def prep(inp):
+        d = dict(perm=float_tensor(inp["permuted"], inp["tokenDtype"]), si=to_dev(inp["sortedIndices"]),
+                 rm=to_dev(inp["routingMap"]), pr=float_tensor(inp["probs"], inp["probsDtype"]))
+        n, T = inp["n"], inp["T"]
+        d["out"] = usc.unpermute_outputs(T, inp["H"], n, inp["tokenDtype"], inp["probsDtype"], "cuda:0")
+        ws = usc.unpermute_workspace_size(inp["permutedRows"], inp["H"], inp["tokenDtype"], n, True,
+                                          inp["probsDtype"], T, inp["Eu"], False)
+        d["ws"] = torch.empty(max(ws, 1), dtype=torch.uint8, device="cuda:0")
+        return d
+
+    da, db = prep(a), prep(b)
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def call(d, st):
+        usc.moe_unpermute(d["perm"], d["si"], d["rm"], d["pr"], padded_mode=False, out=d["out"],
+                          workspace=d["ws"], stream=st)
+
+    # first calls outside any capture create each stream's auxiliary stream
+    call(da, sa)
+    call(db, sb)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=sa, capture_error_mode="thread_local"):
+        call(da, sa)
+        call(db, sb)  # eager, on another stream, during the capture
+    sb.synchronize()
+    assert_unpermute_equal(unpermute_numpy(db["out"], b), oracle.unpermute(b), b)
+    for v in da["out"].values():
+        if v is not None:
+            v.zero_()
+    graph.replay()
+    torch.cuda.synchronize()
+    assert_unpermute_equal(unpermute_numpy(da["out"], a), oracle.unpermute(a), a)
+
+
+def test_many_caller_streams():
+    """Not-padded unpermutes on more caller streams than the library keeps
+    auxiliary streams for (64 per device): past that the sort runs in the
+    caller's stream. Every result must equal the oracle."""
+    inp = w.make_unpermute_topk(T=300, k=6, Eu=24, H=64, dtype=1, probs_dtype=1, choices=(2, 6), seed=63)
+    ref = oracle.unpermute(inp)
+    perm = float_tensor(inp["permuted"], inp["tokenDtype"])
+    si, rm, pr = to_dev(inp["sortedIndices"]), to_dev(inp["routingMap"]), float_tensor(inp["probs"], inp["probsDtype"])
+    streams = [torch.cuda.Stream() for _ in range(72)]
+    outs = []
+    for st in streams:
+        with torch.cuda.stream(st):
+            outs.append(usc.moe_unpermute(perm, si, rm, pr, padded_mode=False))
+    torch.cuda.synchronize()
+    for o in outs:
+        assert_unpermute_equal(unpermute_numpy(o, inp), ref, inp)

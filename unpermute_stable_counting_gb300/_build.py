@@ -3,6 +3,12 @@
 Each translation unit under csrc/ is compiled in parallel with nvcc, then
 linked into one shared library next to this file. No torch headers are
 involved: the library's ABI is plain C (include/moe_reorder.h).
+
+Whether a build is needed is decided by content, not file times: the library
+is stamped with a SHA-256 digest of every source and header it is built from,
+the nvcc flags, the compiler's version and the host machine type, and it is
+rebuilt whenever the stamp is missing or differs. A binary copied in with a
+newer time but from other sources is therefore never reused.
 """
 from __future__ import annotations
 
@@ -10,14 +16,18 @@ import concurrent.futures as fut
 import contextlib
 import fcntl
 import glob
+import hashlib
 import os
+import platform
 import subprocess
+import sys
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(CSRC, "_build")
 LIB_PATH = os.path.join(PKG, "libmoe_reorder.so")
+STAMP_PATH = LIB_PATH + ".sha256"
 HEADER = os.path.join(ROOT, "include", "moe_reorder.h")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -38,11 +48,38 @@ def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [HEADER, __file__]
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB_PATH):
+def _nvcc_version() -> str:
+    try:
+        r = subprocess.run([_nvcc(), "--version"], capture_output=True, text=True)
+        return r.stdout.strip().splitlines()[-1] if r.stdout.strip() else ""
+    except OSError:
+        return ""
+
+
+def source_digest(files, flags, tool_version: str = "", machine: str = "") -> str:
+    """SHA-256 over the files' names (relative to the repository) and contents,
+    the flags, the compiler version and the machine type."""
+    h = hashlib.sha256()
+    for f in sorted(files):
+        h.update(os.path.relpath(f, ROOT).encode() + b"\0")
+        with open(f, "rb") as fh:
+            h.update(fh.read())
+        h.update(b"\0")
+    for x in list(flags) + [tool_version, machine]:
+        h.update(str(x).encode() + b"\0")
+    return h.hexdigest()
+
+
+def current_digest(extra_flags=None) -> str:
+    return source_digest(_deps(), NVCC_FLAGS + list(extra_flags or []), _nvcc_version(),
+                         platform.machine())
+
+
+def needs_build(extra_flags=None) -> bool:
+    if not os.path.exists(LIB_PATH) or not os.path.exists(STAMP_PATH):
         return True
-    t = os.path.getmtime(LIB_PATH)
-    return any(os.path.getmtime(d) > t for d in _deps())
+    with open(STAMP_PATH) as f:
+        return f.read().strip() != current_digest(extra_flags)
 
 
 @contextlib.contextmanager
@@ -58,10 +95,12 @@ def _build_lock():
 
 
 def build_library(force: bool = False, extra_flags: list[str] | None = None) -> str:
-    if not force and not needs_build():
+    if not force and not needs_build(extra_flags):
+        print(f"libmoe_reorder.so: reused (sources unchanged, digest {current_digest(extra_flags)[:16]})",
+              file=sys.stderr)
         return LIB_PATH
     with _build_lock():
-        if not force and not needs_build():
+        if not force and not needs_build(extra_flags):
             return LIB_PATH
         return _build_locked(extra_flags)
 
@@ -85,7 +124,12 @@ def _build_locked(extra_flags: list[str] | None) -> str:
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
+    digest = current_digest(extra_flags)
     os.replace(tmp, LIB_PATH)
+    with open(STAMP_PATH + f".tmp{os.getpid()}", "w") as f:
+        f.write(digest + "\n")
+    os.replace(STAMP_PATH + f".tmp{os.getpid()}", STAMP_PATH)
+    print(f"libmoe_reorder.so: compiled (digest {digest[:16]})", file=sys.stderr)
     return LIB_PATH
 
 

@@ -132,16 +132,24 @@ __host__ __device__ inline uint64_t align_up(uint64_t x, uint64_t a) { return (x
 
 int device_sm_count();                 // cached per device
 
-// Per-device auxiliary stream with fork/join events, created on first use and
-// kept for the process lifetime. `mu` serialises the enqueue of one fork/join
-// sequence, so concurrent host threads do not interleave their records.
+// Auxiliary stream with fork/join events, one per (device, caller stream),
+// created on first use and kept for the process lifetime. `mu` serialises the
+// enqueue of one fork/join sequence, so host threads that share a caller
+// stream do not interleave their records. Calls on different caller streams
+// never share one: their side work overlaps, and a stream capture on one
+// caller stream does not reach the auxiliary stream of another.
+constexpr int kMaxAuxStreams = 64;  // caller streams per device
 struct AuxStream {
+    cudaStream_t caller;
     cudaStream_t stream;
     cudaEvent_t fork;
     cudaEvent_t join;
     std::mutex mu;
 };
-AuxStream* aux_stream();  // for the current device; nullptr on a CUDA error
+// The auxiliary stream of `caller` on the current device; nullptr when the
+// device already has kMaxAuxStreams of them (the caller then runs the side
+// work in line) or on a CUDA error (*err set).
+AuxStream* aux_stream(cudaStream_t caller, cudaError_t* err);
 void profile_mark(cudaStream_t s, int event_index);  // records a timing event if set
 
 // Launch with programmatic stream serialisation (PDL) enabled, or (pdl =

@@ -9,17 +9,26 @@
 // no cudaMalloc, no cudaFree, no allocating library routine.
 //
 // Costs and rules:
-//  * The array (MR_NOALLOC_SCRATCH_BYTES) occupies device memory on every GPU
-//    that loads this library, until the process exits.
+//  * The array (MR_NOALLOC_SCRATCH_BYTES) occupies device memory on a GPU from
+//    the moment the library's code is loaded there until the process exits.
+//    Under CUDA's default lazy module loading that happens at the first call
+//    on the device (the address lookup below loads it), so the first call on
+//    each device may allocate: a caller that must not allocate after its
+//    start-up makes one call per device during start-up (before it reserves
+//    the device's memory), or sets CUDA_MODULE_LOADING=EAGER so that loading
+//    the library loads the array. Later calls allocate nothing.
 //  * Every call on a device shares the one array. Calls whose work overlaps on
 //    the GPU (for example on two streams at once) race on it; callers must
 //    order such calls (one stream, or events between streams).
 //  * The array keeps the last call's contents. The batching kernels write every
 //    scratch word before they read it (the prefix kernel's ticket counter is
-//    reset by the first kernel of each call), so nothing has to be cleared.
+//    reset by the first kernel of each call; the one-launch sort writes its
+//    count matrix before its grid barrier), so nothing has to be cleared.
 //  * The first call on a device looks up the array's device address there
 //    (cudaGetSymbolAddress, with that device current) and caches it. Make that
-//    first call before any stream capture on the device.
+//    first call before any stream capture on the device. The cached address
+//    belongs to the device's context: do not use the library across a
+//    cudaDeviceReset.
 #include <mutex>
 
 #include "common.cuh"

@@ -21,25 +21,43 @@ int device_sm_count() {
     return n;
 }
 
-AuxStream* aux_stream() {
+AuxStream* aux_stream(cudaStream_t caller, cudaError_t* err) {
     static std::mutex create_mu;
-    static AuxStream* streams[64] = {nullptr};
+    static AuxStream* table[64][kMaxAuxStreams] = {{nullptr}};
+    *err = cudaSuccess;
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-    std::lock_guard<std::mutex> lock(create_mu);
-    if (!streams[dev]) {
-        int lo = 0, hi = 0;
-        if (cudaDeviceGetStreamPriorityRange(&lo, &hi) != cudaSuccess) return nullptr;
-        AuxStream* a = new AuxStream();
-        if (cudaStreamCreateWithPriority(&a->stream, cudaStreamNonBlocking, hi) != cudaSuccess ||
-            cudaEventCreateWithFlags(&a->fork, cudaEventDisableTiming) != cudaSuccess ||
-            cudaEventCreateWithFlags(&a->join, cudaEventDisableTiming) != cudaSuccess) {
-            delete a;
-            return nullptr;
-        }
-        streams[dev] = a;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess || dev < 0 || dev >= 64) {
+        *err = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+        return nullptr;
     }
-    return streams[dev];
+    std::lock_guard<std::mutex> lock(create_mu);
+    AuxStream** row = table[dev];
+    int i = 0;
+    for (; i < kMaxAuxStreams && row[i]; ++i)
+        if (row[i]->caller == caller) return row[i];
+    if (i == kMaxAuxStreams) return nullptr;  // table full: side work in line
+    int lo = 0, hi = 0;
+    e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
+    if (e != cudaSuccess) {
+        *err = e;
+        return nullptr;
+    }
+    AuxStream* a = new AuxStream();
+    a->caller = caller;
+    a->stream = nullptr;
+    a->fork = a->join = nullptr;
+    if ((e = cudaStreamCreateWithPriority(&a->stream, cudaStreamNonBlocking, hi)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&a->fork, cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&a->join, cudaEventDisableTiming)) != cudaSuccess) {
+        if (a->fork) cudaEventDestroy(a->fork);
+        if (a->stream) cudaStreamDestroy(a->stream);
+        delete a;
+        *err = e;
+        return nullptr;
+    }
+    row[i] = a;
+    return a;
 }
 
 void profile_mark(cudaStream_t s, int event_index) {

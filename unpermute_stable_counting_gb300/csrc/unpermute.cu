@@ -676,12 +676,13 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
     };
 
     cudaError_t e = cudaSuccess;
-    if (!p.padded) {
+    cudaError_t ea = cudaSuccess;
+    AuxStream* ax = p.padded ? nullptr : aux_stream(s, &ea);
+    if (ea != cudaSuccess) return MR_ERR_CUDA;
+    if (ax) {
         // Not padded, the sort's outputs are not read by the gather-reduce: it
-        // runs on the library's auxiliary stream, forked from and joined back
-        // into the caller's stream, so it overlaps the reduce.
-        AuxStream* ax = aux_stream();
-        if (!ax) return MR_ERR_CUDA;
+        // runs on the auxiliary stream of the caller's stream, forked from and
+        // joined back into it, so it overlaps the reduce.
         std::lock_guard<std::mutex> lock(ax->mu);
         MR_TRY_CUDA(cudaEventRecord(ax->fork, s));
         MR_TRY_CUDA(cudaStreamWaitEvent(ax->stream, ax->fork, 0));
