@@ -490,6 +490,25 @@ int32_t mr_version(void);
  */
 mr_status mr_profile_set_events(void* const* events, int32_t count);
 
+/*
+ * mr_checked_errors -- the bounds checks of a checked build.
+ *   No counterpart on the pages; its nearest relative is the unpermute
+ *   kernel's IsValidInputIndex guard ("MoeTokenUnpermuteWithRoutingMap
+ *   算子全解析", Kernel 实现), which skips a slot whose index is out of range.
+ *   A library built with -DMR_CHECKED range-checks every gather index, row
+ *   offset, CSR row pointer and scatter destination that a kernel derives
+ *   from data (an input, a workspace word or another kernel's output); an
+ *   access that fails its check is skipped and counted in a device error
+ *   word. On valid inputs the count stays 0 and the outputs are those of the
+ *   regular build. This call synchronises with the device, writes the number
+ *   of failed checks since the last reset to *failures (host pointer) and
+ *   the site number of the first one to *firstSite (host pointer, may be
+ *   NULL), and with reset != 0 clears the words.
+ *   Returns MR_OK, MR_ERR_PARAM_NULLPTR (failures NULL), MR_ERR_CUDA, or
+ *   MR_ERR_UNSUPPORTED in a regular build (which has no checks; it writes 0).
+ */
+mr_status mr_checked_errors(uint32_t* failures, uint32_t* firstSite, int32_t reset);
+
 #ifdef __cplusplus
 }
 #endif

@@ -28,6 +28,10 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD_DIR = os.path.join(CSRC, "_build")
 LIB_PATH = os.path.join(PKG, "libmoe_reorder.so")
 STAMP_PATH = LIB_PATH + ".sha256"
+# the bounds-checked build (-DMR_CHECKED): its own objects, library and stamp
+CHECKED_FLAGS = ["-DMR_CHECKED"]
+CHECKED_BUILD_DIR = os.path.join(CSRC, "_build_checked")
+CHECKED_LIB_PATH = os.path.join(PKG, "libmoe_reorder_checked.so")
 HEADER = os.path.join(ROOT, "include", "moe_reorder.h")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -75,11 +79,18 @@ def current_digest(extra_flags=None) -> str:
                          platform.machine())
 
 
-def needs_build(extra_flags=None) -> bool:
-    if not os.path.exists(LIB_PATH) or not os.path.exists(STAMP_PATH):
+def _paths(checked: bool):
+    if checked:
+        return CHECKED_LIB_PATH, CHECKED_LIB_PATH + ".sha256", CHECKED_BUILD_DIR, CHECKED_FLAGS
+    return LIB_PATH, STAMP_PATH, BUILD_DIR, []
+
+
+def needs_build(extra_flags=None, checked: bool = False) -> bool:
+    lib_path, stamp, _, cflags = _paths(checked)
+    if not os.path.exists(lib_path) or not os.path.exists(stamp):
         return True
-    with open(STAMP_PATH) as f:
-        return f.read().strip() != current_digest(extra_flags)
+    with open(stamp) as f:
+        return f.read().strip() != current_digest(cflags + list(extra_flags or []))
 
 
 @contextlib.contextmanager
@@ -94,23 +105,29 @@ def _build_lock():
             fcntl.flock(f, fcntl.LOCK_UN)
 
 
-def build_library(force: bool = False, extra_flags: list[str] | None = None) -> str:
-    if not force and not needs_build(extra_flags):
-        print(f"libmoe_reorder.so: reused (sources unchanged, digest {current_digest(extra_flags)[:16]})",
-              file=sys.stderr)
-        return LIB_PATH
+def build_library(force: bool = False, extra_flags: list[str] | None = None, checked: bool = False) -> str:
+    """Build (or reuse) the library; checked=True builds the bounds-checked
+    variant (-DMR_CHECKED) into its own objects and library file."""
+    lib_path, _, _, cflags = _paths(checked)
+    flags = cflags + list(extra_flags or [])
+    if not force and not needs_build(extra_flags, checked):
+        print(f"{os.path.basename(lib_path)}: reused (sources unchanged, digest "
+              f"{current_digest(flags)[:16]})", file=sys.stderr)
+        return lib_path
     with _build_lock():
-        if not force and not needs_build(extra_flags):
-            return LIB_PATH
-        return _build_locked(extra_flags)
+        if not force and not needs_build(extra_flags, checked):
+            return lib_path
+        return _build_locked(extra_flags, checked)
 
 
-def _build_locked(extra_flags: list[str] | None) -> str:
+def _build_locked(extra_flags: list[str] | None, checked: bool = False) -> str:
+    lib_path, stamp, build_dir, cflags = _paths(checked)
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    flags = NVCC_FLAGS + cflags + list(extra_flags or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -119,18 +136,18 @@ def _build_locked(extra_flags: list[str] | None) -> str:
 
     with fut.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB_PATH + f".tmp{os.getpid()}"
+    tmp = lib_path + f".tmp{os.getpid()}"
     cmd = [nvcc] + ARCH_FLAGS + ["-shared", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"nvcc link failed:\n{r.stdout}\n{r.stderr}")
-    digest = current_digest(extra_flags)
-    os.replace(tmp, LIB_PATH)
-    with open(STAMP_PATH + f".tmp{os.getpid()}", "w") as f:
+    digest = current_digest(cflags + list(extra_flags or []))
+    os.replace(tmp, lib_path)
+    with open(stamp + f".tmp{os.getpid()}", "w") as f:
         f.write(digest + "\n")
-    os.replace(STAMP_PATH + f".tmp{os.getpid()}", STAMP_PATH)
-    print(f"libmoe_reorder.so: compiled (digest {digest[:16]})", file=sys.stderr)
-    return LIB_PATH
+    os.replace(stamp + f".tmp{os.getpid()}", stamp)
+    print(f"{os.path.basename(lib_path)}: compiled (digest {digest[:16]})", file=sys.stderr)
+    return lib_path
 
 
 if __name__ == "__main__":

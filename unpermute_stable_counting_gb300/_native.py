@@ -1,7 +1,9 @@
 """ctypes declarations of the C ABI in include/moe_reorder.h.
 
 Loading fails loudly when libmoe_reorder.so is missing: there is no CPU or
-PyTorch fallback for any operation of this package.
+PyTorch fallback for any operation of this package. With USC_CHECKED=1 in the
+environment the bounds-checked build (libmoe_reorder_checked.so, built with
+-DMR_CHECKED) is loaded instead.
 """
 from __future__ import annotations
 
@@ -44,7 +46,12 @@ SIGNATURES = {
     "mr_status_string": (ctypes.c_char_p, [_I32]),
     "mr_version": (_I32, []),
     "mr_profile_set_events": (_I32, [ctypes.POINTER(_P), _I32]),
+    "mr_checked_errors": (_I32, [ctypes.POINTER(_U32), ctypes.POINTER(_U32), _I32]),
 }
+
+
+def checked_requested() -> bool:
+    return os.environ.get("USC_CHECKED", "") == "1"
 
 _lib = None
 
@@ -57,7 +64,7 @@ def lib(path: str | None = None) -> ctypes.CDLL:
     """The loaded library (loaded once)."""
     global _lib
     if _lib is None:
-        p = path or _build.LIB_PATH
+        p = path or (_build.CHECKED_LIB_PATH if checked_requested() else _build.LIB_PATH)
         if not os.path.exists(p):
             raise LibraryMissing(
                 f"{p} is not built; run unpermute_stable_counting_gb300._build.build_library() "
@@ -69,6 +76,18 @@ def lib(path: str | None = None) -> ctypes.CDLL:
             f.argtypes = args
         _lib = L
     return _lib
+
+
+def checked_errors(reset: bool = True):
+    """(failures, first site) of the bounds checks of a checked build, or None
+    for a regular build."""
+    f, s = _U32(0), _U32(0)
+    st = lib().mr_checked_errors(ctypes.byref(f), ctypes.byref(s), 1 if reset else 0)
+    if st == 561003:  # MR_ERR_UNSUPPORTED: a regular build
+        return None
+    if st != 0:
+        raise RuntimeError(f"mr_checked_errors failed with status {st}")
+    return int(f.value), int(s.value)
 
 
 def int64_array(values) -> ctypes.Array:

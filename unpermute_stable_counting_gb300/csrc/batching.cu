@@ -24,6 +24,10 @@
 
 
 
+namespace mr {
+MR_CHECK_ACCESSOR(batching)
+}  // namespace mr
+
 using namespace mr;
 
 extern "C" mr_status ffnwb_batching_get_workspace_size(int64_t expertNum, const int64_t* maxOutShape,
@@ -81,7 +85,7 @@ extern "C" mr_status ffnwb_batching_ex(const int32_t* expertIds, int32_t layerId
 
     profile_mark(s, 0);
     BatchScatter<BatchKey> sc{kf, row_keys, sessionIdsIn, microBatchIdsIn, tokenIdsIn, sessionIds,
-                              microBatchIds, tokenIds, expertOffsets, gather_idx, sortedIndicesOut};
+                              microBatchIds, tokenIds, expertOffsets, gather_idx, sortedIndicesOut, p.Y};
     MR_TRY_CUDA(batching_index(kf, p.Y, p.B, cs, gl, sc, s));
     profile_mark(s, 1);
     profile_mark(s, 2);
@@ -89,7 +93,7 @@ extern "C" mr_status ffnwb_batching_ex(const int32_t* expertIds, int32_t layerId
                            reinterpret_cast<const uint8_t*>(tokenData), tokenRowStride,
                            p.row_bytes, int8 ? 1 : 0, reinterpret_cast<const uint8_t*>(scales),
                            scaleStride, reinterpret_cast<uint8_t*>(y), dynamicScale, gather_idx,
-                           cs.bucket_start, row_keys, (const uint64_t*)nullptr));
+                           cs.bucket_start, row_keys, (const uint64_t*)nullptr, p.Y));
     profile_mark(s, 3);
     MR_TRY_CUDA(cudaGetLastError());
     return MR_OK;

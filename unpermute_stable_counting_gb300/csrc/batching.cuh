@@ -47,6 +47,7 @@ struct BatchScatter {
     int32_t* eoff_out;
     int32_t* gather_idx;
     int32_t* slot_row;
+    int64_t n;  // slots (and output rows)
     // The slot's ids, loaded apart from the stores (the one-launch sort loads
     // them with the keys).
     struct Pre {
@@ -56,6 +57,7 @@ struct BatchScatter {
         return Pre{sess_in[s], micro_in[s], tok_in ? tok_in[s] : (int32_t)s};
     }
     __device__ __forceinline__ void store(int64_t s, int k, uint32_t d, uint32_t start, const Pre& p) const {
+        if (!MR_IN_RANGE(d, n, 101)) return;
         gather_idx[d] = (int32_t)s;
         const bool routed = k < kf.E;
         const bool has_row = k < src_keys;
@@ -63,7 +65,7 @@ struct BatchScatter {
         micro_out[d] = has_row ? p.micro : -1;
         tok_out[d] = has_row ? p.tok : -1;
         eoff_out[d] = routed ? (int32_t)(d - start) : -1;
-        if (slot_row) slot_row[s] = routed ? (int32_t)d : -1;
+        if (slot_row && MR_IN_RANGE(s, n, 102)) slot_row[s] = routed ? (int32_t)d : -1;
     }
     __device__ __forceinline__ void operator()(int64_t s, int k, uint32_t d, uint32_t start) const {
         Pre p{-1, -1, -1};
@@ -79,6 +81,7 @@ batching_scatter_kernel(KeyFn kf, int64_t Y, int B, CsortBufs cs, BatchScatter<K
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t s = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; s < Y; s += stride) {
         const int k = kf(s);
+        if (!MR_IN_RANGE(k, B, 103)) continue;
         sc(s, k, csort_dest(k, s, cs, B), cs.bucket_start[k]);
     }
 }

@@ -126,6 +126,39 @@ __device__ __forceinline__ float load_f32(const void* base, int64_t i, int dt) {
 }
 
 // ---------------------------------------------------------------------------
+// Bounds-checked build (-DMR_CHECKED). Every gather index, row offset, CSR
+// pointer and scatter destination that a kernel derives from data goes
+// through MR_IN_RANGE(i, n, site): in a checked build it tests 0 <= i < n
+// and, when that fails, counts the failure in this translation unit's error
+// words (with the number of the first failing site) and yields false, so
+// that the caller skips the access. In a regular build it is the constant
+// true and costs nothing. mr_checked_errors() reads and clears the words of
+// every translation unit; each .cu file that launches kernels defines its
+// reader with MR_CHECK_ACCESSOR(name).
+// ---------------------------------------------------------------------------
+#ifdef MR_CHECKED
+static __device__ unsigned int g_mr_check_words[2];  // failures, first failing site
+__device__ __forceinline__ bool mr_in_range(int64_t i, int64_t n, unsigned site) {
+    if (i >= 0 && i < n) return true;
+    if (atomicAdd(&g_mr_check_words[0], 1u) == 0u) atomicExch(&g_mr_check_words[1], site);
+    return false;
+}
+#define MR_IN_RANGE(i, n, site) ::mr::mr_in_range((int64_t)(i), (int64_t)(n), (unsigned)(site))
+#define MR_CHECK_ACCESSOR(name)                                                              \
+    cudaError_t mr_check_words_##name(unsigned* out, bool reset) {                           \
+        cudaError_t e = cudaMemcpyFromSymbol(out, g_mr_check_words, 2 * sizeof(unsigned));    \
+        if (e == cudaSuccess && reset) {                                                     \
+            const unsigned zero[2] = {0u, 0u};                                               \
+            e = cudaMemcpyToSymbol(g_mr_check_words, zero, sizeof(zero));                    \
+        }                                                                                    \
+        return e;                                                                            \
+    }
+#else
+#define MR_IN_RANGE(i, n, site) true
+#define MR_CHECK_ACCESSOR(name)
+#endif
+
+// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 __host__ __device__ inline uint64_t align_up(uint64_t x, uint64_t a) { return (x + a - 1) / a * a; }

@@ -113,6 +113,7 @@ context_parse_kernel(const uint8_t* __restrict__ ctx, int64_t Y, int32_t El, int
         const int32_t m_id = (int32_t)(b % v.micro);
         for (int64_t j = lane; j < v.per_block; j += 32) {
             const int64_t g = b * v.per_block + j;
+            if (!MR_IN_RANGE(g, Y, 801)) continue;
             const int32_t id = desc[2 + j];
             keys[g] = (layer_ok && id >= 0 && id < El) ? layer * El + id : E;
             sess[g] = s_id;
@@ -141,6 +142,8 @@ static mr_status plan_context(int64_t expertNum, const int64_t* maxOutShape, int
     *ws = p->ws_bytes + 3 * align_up((uint64_t)p->Y * 4u, 256) + csort_coop_bytes(p->Y, p->B);
     return MR_OK;
 }
+
+MR_CHECK_ACCESSOR(context)
 
 }  // namespace mr
 
@@ -212,7 +215,7 @@ extern "C" mr_status ffnwb_batching_context_ex(
     KeyArray kf{keys, (int32_t)p.E};
     GroupListOut gl{groupList, actualTokenNum, (int)p.E};
     BatchScatter<KeyArray> sc{kf, row_keys, sess, micro, nullptr, sessionIds, microBatchIds, tokenIds,
-                              expertOffsets, gather_idx, nullptr};
+                              expertOffsets, gather_idx, nullptr, p.Y};
     MR_TRY_CUDA(batching_index(kf, p.Y, p.B, cs, gl, sc, s));
     profile_mark(s, 1);
     profile_mark(s, 2);
@@ -221,7 +224,7 @@ extern "C" mr_status ffnwb_batching_context_ex(
                            (const uint8_t*)nullptr, (int64_t)4, reinterpret_cast<uint8_t*>(y),
                            dynamicScale, (const int32_t*)gather_idx,
                            (const uint32_t*)cs.bucket_start, row_keys,
-                           reinterpret_cast<const uint64_t*>(ctx + kCtxTokenDataField)));
+                           reinterpret_cast<const uint64_t*>(ctx + kCtxTokenDataField), p.Y));
     profile_mark(s, 3);
     MR_TRY_CUDA(cudaGetLastError());
     return MR_OK;

@@ -102,6 +102,7 @@ csort_rank_kernel(KeyFn kf, int64_t N, int B, uint16_t* __restrict__ tile_rank,
     for (int c = 0; c < kSortChunks; ++c) {
         const int64_t i = base + c * 32 + lane;
         key[c] = i < N ? kf(i) : -1;
+        if (key[c] >= 0 && !MR_IN_RANGE(key[c], B, 201)) key[c] = -1;
     }
     __syncthreads();
 
@@ -223,7 +224,7 @@ csort_prefix_kernel(uint32_t* __restrict__ tile_off, int64_t tiles, int B,
             const int i = i0 + q;
             if (i < c1) {
                 bucket_start[i] = run;
-                if (gl.rows && i < gl.limit && v[q] != 0u) {
+                if (gl.rows && i < gl.limit && v[q] != 0u && MR_IN_RANGE(r, gl.limit, 202)) {
                     gl.rows[2 * (int64_t)r] = i;
                     gl.rows[2 * (int64_t)r + 1] = v[q];
                     ++r;
@@ -304,6 +305,7 @@ csort_single_tile_kernel(KeyFn kf, int64_t Y, int B, uint32_t* __restrict__ buck
     for (int c = 0; c < kSortChunks; ++c) {
         const int64_t i = base + c * 32 + lane;
         key[c] = i < Y ? kf(i) : -1;
+        if (key[c] >= 0 && !MR_IN_RANGE(key[c], B, 203)) key[c] = -1;
     }
     __syncthreads();
     uint16_t* mytab = tab + warp * B;
@@ -352,7 +354,7 @@ csort_single_tile_kernel(KeyFn kf, int64_t Y, int B, uint32_t* __restrict__ buck
         const uint32_t v = bs[k];
         bs[k] = run;
         bucket_start[k] = run;
-        if (gl.rows && k < gl.limit && v != 0u) {
+        if (gl.rows && k < gl.limit && v != 0u && MR_IN_RANGE(r, gl.limit, 204)) {
             gl.rows[2 * (int64_t)r] = k;
             gl.rows[2 * (int64_t)r + 1] = v;
             ++r;

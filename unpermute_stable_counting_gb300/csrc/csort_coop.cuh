@@ -118,7 +118,7 @@ __device__ __forceinline__ void coop_scan_starts(uint32_t* st, int B, bool write
         st[k] = run;
         if (write) {
             bucket_start[k] = run;
-            if (gl.rows && k < gl.limit && v != 0u) {
+            if (gl.rows && k < gl.limit && v != 0u && MR_IN_RANGE(r, gl.limit, 206)) {
                 gl.rows[2 * (int64_t)r] = k;
                 gl.rows[2 * (int64_t)r + 1] = v;
                 ++r;
@@ -168,6 +168,7 @@ csort_coop_kernel(KeyFn kf, int64_t N, int B, uint32_t* __restrict__ counts_t,
     for (int c = 0; c < kCoopChunks; ++c) {
         const int64_t i = base + c * 32 + lane;
         key[c] = i < N ? kf(i) : -1;
+        if (key[c] >= 0 && !MR_IN_RANGE(key[c], B, 205)) key[c] = -1;
         if (i < N) pre[c] = sc.load(i);
     }
     __syncthreads();

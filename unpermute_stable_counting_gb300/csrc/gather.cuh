@@ -122,14 +122,15 @@ batching_gather_kernel(const uint8_t* __restrict__ token_data_arg, int64_t row_s
                        int64_t scale_stride, uint8_t* __restrict__ y, float* __restrict__ dyn,
                        const int32_t* __restrict__ gather_idx,
                        const uint32_t* __restrict__ bucket_start, int row_keys,
-                       const uint64_t* __restrict__ token_data_loc) {
+                       const uint64_t* __restrict__ token_data_loc, int64_t nrows) {
     pdl_enter();
     // the token rows' address, passed directly or read from device memory
     const uint8_t* __restrict__ token_data =
         token_data_loc ? reinterpret_cast<const uint8_t*>(*token_data_loc) : token_data_arg;
     // rows of the keys below row_keys: the routed rows (row_keys = E), or
     // every row with a token row behind it (the whole-tail option)
-    const uint32_t U = bucket_start[row_keys];
+    uint32_t U = bucket_start[row_keys];
+    if (!MR_IN_RANGE(U, nrows + 1, 301)) U = 0u;
     const int lane = threadIdx.x & 31;
     const bool base16 = (reinterpret_cast<uintptr_t>(token_data) & 15u) == 0u;
     const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -139,6 +140,7 @@ batching_gather_kernel(const uint8_t* __restrict__ token_data_arg, int64_t row_s
     for (int64_t i = gw; i < (int64_t)U; i += nw) {
         const int64_t g = gnext;
         gnext = i + nw < (int64_t)U ? gather_idx[i + nw] : 0;
+        if (!MR_IN_RANGE(g, nrows, 302)) continue;
         warp_copy_row<VPT>(token_data + g * row_stride, y + i * row_bytes, row_bytes, lane, base16);
         if (is_int8) {
             const uint8_t* sp = scales ? scales + g * scale_stride : token_data + g * row_stride + row_bytes;

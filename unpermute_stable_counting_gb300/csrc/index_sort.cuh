@@ -86,7 +86,9 @@ struct RadixScatter {
     PaddedProbs pprobs;
     int32_t* final_index;
     int32_t* final_ptid;
+    int64_t n;  // entries (and positions)
     __device__ __forceinline__ void operator()(int64_t i, int, uint32_t d, uint32_t) const {
+        if (!MR_IN_RANGE(d, n, 501)) return;
         if (pprobs.pp) {
             // permuteProbs[i] = probs[sortedIndices[i], i // capacity], 0 if invalid
             const int32_t v = kf.si[i];
@@ -119,6 +121,7 @@ radix_scatter_kernel(RadixKey kf, int64_t n, int B, CsortBufs cs, RadixScatter s
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
         const int digit = kf(i);
+        if (!MR_IN_RANGE(digit, B, 502)) continue;
         sc(i, digit, csort_dest(digit, i, cs, B), 0u);
     }
 }
@@ -152,7 +155,7 @@ __device__ __forceinline__ void fine_sort_bucket(int c, uint32_t lo, uint32_t hi
                                                  const int32_t* __restrict__ idx, int shift, int64_t T,
                                                  int64_t topk, const int32_t* __restrict__ si,
                                                  int32_t* __restrict__ out_index, int32_t* __restrict__ ptid,
-                                                 int32_t* __restrict__ ptr, uint32_t* fsm) {
+                                                 int32_t* __restrict__ ptr, uint32_t* fsm, int64_t n) {
     const int F = 1 << shift;
     uint32_t* hist = fsm;                     // [F] counts, then fine starts
     uint32_t* running = fsm + F;              // [F] items placed so far
@@ -197,9 +200,11 @@ __device__ __forceinline__ void fine_sort_bucket(int c, uint32_t lo, uint32_t hi
             uint32_t r = below + running[f] + hist[f];
             for (int w = 0; w < warp; ++w) r += wcnt[w * F + f];
             const uint32_t pos = lo + r;
-            out_index[pos] = o;
-            // padded, a valid entry's full key is its value sortedIndices[o]
-            ptid[pos] = PADDED ? (int32_t)(fk) : (int32_t)(o / topk);
+            if (MR_IN_RANGE(pos, hi, 503) && MR_IN_RANGE(o, n, 504)) {
+                out_index[pos] = o;
+                // padded, a valid entry's full key is its value sortedIndices[o]
+                ptid[pos] = PADDED ? (int32_t)(fk) : (int32_t)(o / topk);
+            }
         }
         __syncthreads();
         if (leader) {
@@ -215,12 +220,14 @@ __global__ void __launch_bounds__(kFineThreads)
 fine_sort_kernel(const uint32_t* __restrict__ keys, const int32_t* __restrict__ idx,
                  const uint32_t* __restrict__ cstart, int shift, int64_t T, int64_t topk,
                  const int32_t* __restrict__ si, int32_t* __restrict__ out_index,
-                 int32_t* __restrict__ ptid, int32_t* __restrict__ ptr) {
+                 int32_t* __restrict__ ptid, int32_t* __restrict__ ptr, int64_t n) {
     extern __shared__ __align__(16) uint32_t fsm[];
     pdl_enter();
     const int c = PADDED ? (int)blockIdx.x : (int)blockIdx.x + 1;
-    fine_sort_bucket<PADDED>(c, cstart[c], cstart[c + 1], c == (int)gridDim.x - 1, keys, idx, shift, T,
-                             topk, si, out_index, ptid, ptr, fsm);
+    uint32_t lo = cstart[c], hi = cstart[c + 1];
+    if (!MR_IN_RANGE(hi, n + 1, 505) || !MR_IN_RANGE(lo, (int64_t)hi + 1, 506)) lo = hi = 0u;
+    fine_sort_bucket<PADDED>(c, lo, hi, c == (int)gridDim.x - 1, keys, idx, shift, T, topk, si, out_index,
+                             ptid, ptr, fsm, n);
 }
 
 // ptr[t] = first position of the sorted keys with key >= t, t in [0, T].

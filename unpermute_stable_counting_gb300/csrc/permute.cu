@@ -54,7 +54,8 @@ __device__ __forceinline__ int64_t permute_pair_row(const int8_t* __restrict__ m
             if (j < topk) si[t * topk + j] = (int32_t)row;
         } else if (rank < cap) {
             row = e * cap + rank;
-            si[row] = (int32_t)t;
+            if (MR_IN_RANGE(row, n, 601)) si[row] = (int32_t)t;
+            else row = -1;
         }
     }
     j_base += __popc(bal);
@@ -245,6 +246,8 @@ static int permute_grid(int64_t units) {
     const int64_t cap = (int64_t)device_sm_count() * 8;
     return (int)(want < 1 ? 1 : (want < cap ? want : cap));
 }
+
+MR_CHECK_ACCESSOR(permute)
 
 }  // namespace mr
 

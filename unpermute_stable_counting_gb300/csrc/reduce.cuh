@@ -46,7 +46,7 @@ __device__ __forceinline__ int build_list(int64_t c0, int64_t c1, const int32_t*
         if (e < c1) {
             if (PADDED) {
                 r = out_index[e];
-                keep = true;
+                keep = MR_IN_RANGE(r, rows, 401);
             } else {
                 const int32_t v = si[e];
                 keep = v >= 0 && (int64_t)v < rows;
@@ -173,7 +173,8 @@ __device__ __forceinline__ void small_map_build(const SmallMap& sm, int64_t T, u
 // and its value.
 template <int PDT>
 __device__ __forceinline__ float small_map_weight(const SmallMap& sm, const uint32_t* smask,
-                                                  const uint32_t* sstart, int64_t i, int64_t& src) {
+                                                  const uint32_t* sstart, int64_t i, int64_t T,
+                                                  int64_t& src) {
     const int64_t Eu = sm.Eu;
     if (i >= (int64_t)sstart[Eu]) {
         src = -1;
@@ -189,9 +190,14 @@ __device__ __forceinline__ float small_map_weight(const SmallMap& sm, const uint
     int64_t w = 0;
     uint32_t m = smask[lo];
     uint32_t c = (uint32_t)__popc(m);
+    const int64_t nb = (T + 31) / 32;
     while (r >= c) {  // the column holds more than r routed tokens
         r -= c;
         ++w;
+        if (!MR_IN_RANGE(w, nb, 406)) {
+            src = -1;
+            return 0.0f;
+        }
         m = smask[w * Eu + lo];
         c = (uint32_t)__popc(m);
     }
@@ -246,6 +252,8 @@ unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows,
         if (PADDED) {
             L0 = ptr[t];
             L1 = ptr[t + 1];
+            // row pointers: 0 <= L0 <= L1 <= rows (padded: one entry per row)
+            if (!MR_IN_RANGE(L1, rows + 1, 404) || !MR_IN_RANGE(L1 - L0, L1 + 1, 405)) L0 = L1 = 0;
         } else {
             L0 = t * topk;
             L1 = L0 + topk;
@@ -260,7 +268,7 @@ unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows,
                 int64_t r;
                 if (PADDED) {
                     r = out_index[e];
-                    keep0 = true;
+                    keep0 = MR_IN_RANGE(r, rows, 402);
                 } else {
                     const int32_t v = si[e];
                     keep0 = v >= 0 && (int64_t)v < rows;
@@ -268,7 +276,7 @@ unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows,
                 }
                 if constexpr (SMALL) {
                     int64_t src;
-                    const float ws = small_map_weight<PDT>(smap, smask, sstart, e, src);
+                    const float ws = small_map_weight<PDT>(smap, smask, sstart, e, T, src);
                     if (c0 == 0) small_map_store<PDT>(smap, e, src);
                     if (keep0) {
                         w0 = ws;
@@ -303,7 +311,7 @@ unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows,
                     int64_t r;
                     if (PADDED) {
                         r = out_index[e];
-                        keep = true;
+                        keep = MR_IN_RANGE(r, rows, 403);
                     } else {
                         const int32_t v = si[e];
                         keep = v >= 0 && (int64_t)v < rows;
@@ -311,7 +319,7 @@ unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows,
                     }
                     if constexpr (SMALL) {
                         int64_t src;
-                        const float ws = small_map_weight<PDT>(smap, smask, sstart, e, src);
+                        const float ws = small_map_weight<PDT>(smap, smask, sstart, e, T, src);
                         if (c == 0) small_map_store<PDT>(smap, e, src);
                         if (keep) {
                             w = ws;
@@ -398,6 +406,8 @@ unpermute_reduce_scalar_kernel(const uint8_t* __restrict__ permuted, int64_t row
         if (PADDED) {
             L0 = ptr[t];
             L1 = ptr[t + 1];
+            // row pointers: 0 <= L0 <= L1 <= rows (padded: one entry per row)
+            if (!MR_IN_RANGE(L1, rows + 1, 404) || !MR_IN_RANGE(L1 - L0, L1 + 1, 405)) L0 = L1 = 0;
         } else {
             L0 = t * topk;
             L1 = L0 + topk;

@@ -79,6 +79,40 @@ extern "C" const char* mr_status_string(mr_status status) {
     return "unknown status";
 }
 
+#ifdef MR_CHECKED
+namespace mr {
+cudaError_t mr_check_words_batching(unsigned* out, bool reset);
+cudaError_t mr_check_words_context(unsigned* out, bool reset);
+cudaError_t mr_check_words_permute(unsigned* out, bool reset);
+cudaError_t mr_check_words_unpermute(unsigned* out, bool reset);
+cudaError_t mr_check_words_update_expert(unsigned* out, bool reset);
+}  // namespace mr
+#endif
+
+extern "C" mr_status mr_checked_errors(uint32_t* failures, uint32_t* firstSite, int32_t reset) {
+#ifdef MR_CHECKED
+    if (!failures) return MR_ERR_PARAM_NULLPTR;
+    cudaError_t (*readers[])(unsigned*, bool) = {mr::mr_check_words_batching, mr::mr_check_words_context,
+                                                 mr::mr_check_words_permute, mr::mr_check_words_unpermute,
+                                                 mr::mr_check_words_update_expert};
+    uint32_t total = 0u, first = 0u;
+    for (auto rd : readers) {
+        unsigned w[2] = {0u, 0u};
+        if (rd(w, reset != 0) != cudaSuccess) return MR_ERR_CUDA;
+        if (w[0] != 0u && first == 0u) first = w[1];
+        total += w[0];
+    }
+    *failures = total;
+    if (firstSite) *firstSite = first;
+    return MR_OK;
+#else
+    (void)reset;
+    if (failures) *failures = 0u;
+    if (firstSite) *firstSite = 0u;
+    return MR_ERR_UNSUPPORTED;
+#endif
+}
+
 extern "C" int32_t mr_version(void) { return 100; }
 
 extern "C" mr_status mr_profile_set_events(void* const* events, int32_t count) {

@@ -498,6 +498,8 @@ static cudaError_t launch_mask_select(const UnpermutePlan& p, const int8_t* map,
     return cudaLaunchKernelEx(&cfg, mask_select_kernel, map, p.T, p.Eu, p.n, probs, p.pes, tile_cnt, pp);
 }
 
+MR_CHECK_ACCESSOR(unpermute)
+
 }  // namespace mr
 
 using namespace mr;
@@ -588,7 +590,7 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
             RadixScatter sc{kf, iin, keys[pass & 1], last ? nullptr : idx[pass & 1],
                             last ? outIndex : nullptr, last ? permuteTokenId : nullptr,
                             p.topk > 0 ? p.topk : (int64_t)1, ppr,
-                            apart ? outIndex : nullptr, apart ? permuteTokenId : nullptr};
+                            apart ? outIndex : nullptr, apart ? permuteTokenId : nullptr, p.n};
             cudaError_t e;
             if (p.n <= kSortTile) {
                 e = csort_single_tile(kf, p.n, B, cs, none, sc, ss);  // one block
@@ -614,7 +616,7 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
             return launch_pdl(kern, dim3((unsigned)blocks), dim3(kFineThreads), smem, ss,
                               (const uint32_t*)kin, (const int32_t*)iin, (const uint32_t*)cs.bucket_start,
                               p.fine_bits, p.T, p.topk > 0 ? p.topk : (int64_t)1, sortedIndices, outIndex,
-                              permuteTokenId, ptr);
+                              permuteTokenId, ptr, p.n);
         }
         if (p.padded && p.passes > 1) {
             return launch_pdl(csr_from_keys_kernel, dim3(elementwise_grid(p.n + 1)), dim3(256), 0,

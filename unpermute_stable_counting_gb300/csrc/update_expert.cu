@@ -58,6 +58,8 @@ __global__ void __launch_bounds__(256)
     }
 }
 
+MR_CHECK_ACCESSOR(update_expert)
+
 }  // namespace mr
 
 using namespace mr;
