@@ -89,11 +89,19 @@ extern "C" mr_status ffnwb_batching_ex(const int32_t* expertIds, int32_t layerId
     MR_TRY_CUDA(batching_index(kf, p.Y, p.B, cs, gl, sc, s));
     profile_mark(s, 1);
     profile_mark(s, 2);
-    MR_TRY_CUDA(launch_pdl(batching_gather_kernel<7>, dim3(gather_grid(p.Y)), dim3(256), 0, s,
-                           reinterpret_cast<const uint8_t*>(tokenData), tokenRowStride,
-                           p.row_bytes, int8 ? 1 : 0, reinterpret_cast<const uint8_t*>(scales),
-                           scaleStride, reinterpret_cast<uint8_t*>(y), dynamicScale, gather_idx,
-                           cs.bucket_start, row_keys, (const uint64_t*)nullptr, p.Y));
+    const uint8_t* td = reinterpret_cast<const uint8_t*>(tokenData);
+    const uint8_t* sp = reinterpret_cast<const uint8_t*>(scales);
+    uint8_t* yb = reinterpret_cast<uint8_t*>(y);
+    if (gather_flat_ok(tokenData, tokenRowStride, p.row_bytes, y, int8 ? scales : nullptr, scaleStride, p.Y)) {
+        MR_TRY_CUDA(launch_pdl(batching_gather_flat_kernel, dim3(gather_flat_grid(p.Y, p.row_bytes)),
+                               dim3(kGatherThreads), 0, s, td, tokenRowStride, p.row_bytes, int8 ? 1 : 0, sp,
+                               scaleStride, yb, dynamicScale, (const int32_t*)gather_idx,
+                               (const uint32_t*)cs.bucket_start, row_keys, p.Y));
+    } else {
+        MR_TRY_CUDA(launch_pdl(batching_gather_kernel<7>, dim3(gather_grid(p.Y)), dim3(256), 0, s, td,
+                               tokenRowStride, p.row_bytes, int8 ? 1 : 0, sp, scaleStride, yb, dynamicScale,
+                               gather_idx, cs.bucket_start, row_keys, (const uint64_t*)nullptr, p.Y));
+    }
     profile_mark(s, 3);
     MR_TRY_CUDA(cudaGetLastError());
     return MR_OK;
