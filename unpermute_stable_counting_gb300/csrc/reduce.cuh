@@ -190,11 +190,10 @@ __device__ __forceinline__ float small_map_weight(const SmallMap& sm, const uint
     int64_t w = 0;
     uint32_t m = smask[lo];
     uint32_t c = (uint32_t)__popc(m);
-    const int64_t nb = (T + 31) / 32;
     while (r >= c) {  // the column holds more than r routed tokens
         r -= c;
         ++w;
-        if (!MR_IN_RANGE(w, nb, 406)) {
+        if (!MR_IN_RANGE(w, (T + 31) / 32, 406)) {
             src = -1;
             return 0.0f;
         }
