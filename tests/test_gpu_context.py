@@ -30,8 +30,9 @@ def _built():
 
 
 def device_context(*, sessions, micro, mbs, sel, E, H, dtype, ids, layers=0, flags=1, layerNum=1,
-                   seed=0, data=None):
-    """Device buffers + a device copy of the packed context pointing at them.
+                   seed=0, data=None, base_offset=0):
+    """Device buffers + a device copy of the packed context pointing at them
+    (the token rows base_offset bytes into their allocation).
     Returns (ctx_dev, host pieces for the oracle, keep-alive tensors)."""
     dev = torch.device("cuda:0")
     info = w.make_token_info(sessions=sessions, micro=micro, mbs=mbs, sel=sel, expert_ids=ids,
@@ -41,11 +42,13 @@ def device_context(*, sessions, micro, mbs, sel, E, H, dtype, ids, layers=0, fla
     if data is None:
         data = np.random.default_rng(seed).integers(0, 256, size=slots * stride, dtype=np.uint8)
     info_d = torch.from_numpy(info).to(dev)
-    data_d = torch.from_numpy(np.ascontiguousarray(data)).to(dev)
+    padded = np.zeros(data.size + base_offset, dtype=np.uint8)
+    padded[base_offset:] = data
+    data_d = torch.from_numpy(padded).to(dev)
     El = E // max(layerNum, 1)
     ctx = w.pack_schedule_context(sessions=sessions, micro=micro, mbs=mbs, sel=sel, expert_num=El,
                                   info_ptr=info_d.data_ptr(), info_size=info.size,
-                                  data_ptr=data_d.data_ptr(), data_size=data.size)
+                                  data_ptr=data_d.data_ptr() + base_offset, data_size=data.size)
     ctx_d = torch.from_numpy(ctx).to(dev)
     return ctx_d, (ctx, info, data), (info_d, data_d)
 
@@ -95,6 +98,21 @@ def test_random_contexts(dtype, layers, L, seed):
                                        dtype=dtype, ids=ids, layers=lay, layerNum=L, seed=seed)
     # outputs sized larger than the context's slots: the extra rows are tail
     run_both(ctx_d, host, (sessions + 2, micro * mbs, sel, H), E, dtype, 0, layerNum=L)
+
+
+@pytest.mark.parametrize("dtype,off", [(1, 0), (1, 2), (1, 4), (1, 8), (0, 12), (2, 0), (2, 4)])
+def test_token_buffer_alignment(dtype, off):
+    # 16-bit rows of 8 KB over 1152 slots take the flat gather, whose source
+    # address is read on the device and checked there: an aligned base, and
+    # bases 2 to 12 bytes past a 16-byte boundary (the word and byte forms);
+    # INT8 rows with their scale stay with the warp kernel
+    sessions, micro, mbs, sel, H = 4, 2, 16, 9, 4096
+    rng = np.random.default_rng(40 + off)
+    slots = sessions * micro * mbs * sel
+    ids = rng.integers(-1, 66, size=slots).astype(np.int32)
+    ctx_d, host, keep = device_context(sessions=sessions, micro=micro, mbs=mbs, sel=sel, E=64, H=H,
+                                       dtype=dtype, ids=ids, seed=off, base_offset=off)
+    run_both(ctx_d, host, (sessions, micro * mbs, sel, H), 64, dtype, 0)
 
 
 def test_need_schedule_all_ready():

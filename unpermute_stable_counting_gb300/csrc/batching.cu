@@ -96,7 +96,7 @@ extern "C" mr_status ffnwb_batching_ex(const int32_t* expertIds, int32_t layerId
         MR_TRY_CUDA(launch_pdl(batching_gather_flat_kernel, dim3(gather_flat_grid(p.Y, p.row_bytes)),
                                dim3(kGatherThreads), 0, s, td, tokenRowStride, p.row_bytes, int8 ? 1 : 0, sp,
                                scaleStride, yb, dynamicScale, (const int32_t*)gather_idx,
-                               (const uint32_t*)cs.bucket_start, row_keys, p.Y));
+                               (const uint32_t*)cs.bucket_start, row_keys, (const uint64_t*)nullptr, p.Y));
     } else {
         MR_TRY_CUDA(launch_pdl(batching_gather_kernel<7>, dim3(gather_grid(p.Y)), dim3(256), 0, s, td,
                                tokenRowStride, p.row_bytes, int8 ? 1 : 0, sp, scaleStride, yb, dynamicScale,

@@ -219,12 +219,24 @@ extern "C" mr_status ffnwb_batching_context_ex(
     MR_TRY_CUDA(batching_index(kf, p.Y, p.B, cs, gl, sc, s));
     profile_mark(s, 1);
     profile_mark(s, 2);
-    MR_TRY_CUDA(launch_pdl(batching_gather_kernel<7>, dim3(gather_grid(p.Y)), dim3(256), 0, s,
-                           (const uint8_t*)nullptr, row_stride, p.row_bytes, int8 ? 1 : 0,
-                           (const uint8_t*)nullptr, (int64_t)4, reinterpret_cast<uint8_t*>(y),
-                           dynamicScale, (const int32_t*)gather_idx,
-                           (const uint32_t*)cs.bucket_start, row_keys,
-                           reinterpret_cast<const uint64_t*>(ctx + kCtxTokenDataField), p.Y));
+    // the token rows' address is the context's token_data_buf, read on the
+    // device; 16-byte rows take the flat gather (which checks the address's
+    // alignment itself), INT8 rows with their interleaved scale the warp kernel
+    const uint64_t* td_loc = reinterpret_cast<const uint64_t*>(ctx + kCtxTokenDataField);
+    uint8_t* yb = reinterpret_cast<uint8_t*>(y);
+    if (!int8 && gather_flat_ok_device_base(row_stride, p.row_bytes, y, p.Y)) {
+        MR_TRY_CUDA(launch_pdl(batching_gather_flat_kernel, dim3(gather_flat_grid(p.Y, p.row_bytes)),
+                               dim3(kGatherThreads), 0, s, (const uint8_t*)nullptr, row_stride, p.row_bytes, 0,
+                               (const uint8_t*)nullptr, (int64_t)4, yb, dynamicScale,
+                               (const int32_t*)gather_idx, (const uint32_t*)cs.bucket_start, row_keys, td_loc,
+                               p.Y));
+    } else {
+        MR_TRY_CUDA(launch_pdl(batching_gather_kernel<7>, dim3(gather_grid(p.Y)), dim3(256), 0, s,
+                               (const uint8_t*)nullptr, row_stride, p.row_bytes, int8 ? 1 : 0,
+                               (const uint8_t*)nullptr, (int64_t)4, yb, dynamicScale,
+                               (const int32_t*)gather_idx, (const uint32_t*)cs.bucket_start, row_keys,
+                               td_loc, p.Y));
+    }
     profile_mark(s, 3);
     MR_TRY_CUDA(cudaGetLastError());
     return MR_OK;

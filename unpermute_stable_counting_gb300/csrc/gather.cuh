@@ -168,20 +168,67 @@ batching_gather_kernel(const uint8_t* __restrict__ token_data_arg, int64_t row_s
 // Rows that are only 4-byte aligned (INT8 rows with their interleaved scale)
 // stay with the warp kernel, whose shuffles build the shifted vectors: flat
 // forms of that path measured 55-65 us against 38.8 us for the INT8 workload.
+// The rows' address is passed directly, or read from device memory (a
+// ScheduleContext's token buffer), in which case the host cannot check its
+// alignment and a base that is not 16-byte aligned takes a word-by-word form
+// of the same loop.
 constexpr int kGatherVPT = 4;
 constexpr int kGatherThreads = 256;
 
+// One 4-byte word, and one 16-byte vector, from a source of any alignment
+// (4-byte words when the address allows, else bytes).
+__device__ __forceinline__ uint32_t ld_u32_any(const uint8_t* p) {
+    if ((reinterpret_cast<uintptr_t>(p) & 3u) == 0u) return ld_stream_u32(p);
+    return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+__device__ __forceinline__ uint4 ld_stream_v4_any(const uint8_t* p) {
+    return make_uint4(ld_u32_any(p), ld_u32_any(p + 4), ld_u32_any(p + 8), ld_u32_any(p + 12));
+}
+
+// The flat loop for a source base that turned out not to be 16-byte aligned
+// (read from device memory, as from a ScheduleContext): the same vectors, one
+// at a time, through ld_stream_v4_any.
+static __device__ __noinline__ void gather_flat_unaligned(
+    const uint8_t* __restrict__ token_data, int64_t row_stride, int64_t row_bytes, int is_int8,
+    const uint8_t* __restrict__ scales, int64_t scale_stride, uint8_t* __restrict__ y, float* __restrict__ dyn,
+    const int32_t* __restrict__ gather_idx, int64_t total, int64_t nvec, int64_t nrows) {
+    constexpr int64_t per_block = (int64_t)kGatherThreads * kGatherVPT;
+    for (int64_t b0 = (int64_t)blockIdx.x * per_block; b0 < total; b0 += (int64_t)gridDim.x * per_block) {
+        for (int u = 0; u < kGatherVPT; ++u) {
+            const int64_t v = b0 + (int64_t)u * kGatherThreads + threadIdx.x;
+            if (v >= total) break;
+            const int64_t row = v / nvec;
+            const int64_t o = v - row * nvec;
+            const int64_t g = gather_idx[row];
+            if (!MR_IN_RANGE(g, nrows, 305)) continue;
+            st_stream_v4(y + row * row_bytes + 16 * o, ld_stream_v4_any(token_data + g * row_stride + 16 * o));
+            if (is_int8 && o == 0) {
+                const uint8_t* sp = scales ? scales + g * scale_stride : token_data + g * row_stride + row_bytes;
+                dyn[row] = __uint_as_float(ld_u32_any(sp));
+            }
+        }
+    }
+}
+
 static __global__ void __launch_bounds__(kGatherThreads, 6)
-batching_gather_flat_kernel(const uint8_t* __restrict__ token_data, int64_t row_stride, int64_t row_bytes,
+batching_gather_flat_kernel(const uint8_t* __restrict__ token_data_arg, int64_t row_stride, int64_t row_bytes,
                             int is_int8, const uint8_t* __restrict__ scales, int64_t scale_stride,
                             uint8_t* __restrict__ y, float* __restrict__ dyn,
                             const int32_t* __restrict__ gather_idx, const uint32_t* __restrict__ bucket_start,
-                            int row_keys, int64_t nrows) {
+                            int row_keys, const uint64_t* __restrict__ token_data_loc, int64_t nrows) {
     pdl_enter();
+    // the token rows' address, passed directly or read from device memory
+    const uint8_t* __restrict__ token_data =
+        token_data_loc ? reinterpret_cast<const uint8_t*>(*token_data_loc) : token_data_arg;
     uint32_t U = bucket_start[row_keys];
     if (!MR_IN_RANGE(U, nrows + 1, 303)) U = 0u;
     const int64_t nvec = row_bytes >> 4;
     const int64_t total = (int64_t)U * nvec;
+    if ((reinterpret_cast<uintptr_t>(token_data) & 15u) != 0u) {
+        gather_flat_unaligned(token_data, row_stride, row_bytes, is_int8, scales, scale_stride, y, dyn,
+                              gather_idx, total, nvec, nrows);
+        return;
+    }
     constexpr int64_t per_block = (int64_t)kGatherThreads * kGatherVPT;
     for (int64_t b0 = (int64_t)blockIdx.x * per_block; b0 < total; b0 += (int64_t)gridDim.x * per_block) {
         const int64_t v0 = b0 + threadIdx.x;
@@ -228,6 +275,14 @@ inline bool gather_flat_ok(const void* token_data, int64_t row_stride, int64_t r
     if ((row_bytes & 15) != 0 || (row_stride & 15) != 0) return false;
     if (((reinterpret_cast<uintptr_t>(y) | reinterpret_cast<uintptr_t>(token_data)) & 15u) != 0) return false;
     if (scales && (((reinterpret_cast<uintptr_t>(scales) | (uintptr_t)scale_stride) & 3u) != 0)) return false;
+    return rows * (row_bytes >> 4) >= kGatherFlatMinVectors;
+}
+
+// The same for rows whose address the kernel reads from device memory: the
+// host checks the shape and y; the kernel checks the base (see above).
+inline bool gather_flat_ok_device_base(int64_t row_stride, int64_t row_bytes, const void* y, int64_t rows) {
+    if ((row_bytes & 15) != 0 || (row_stride & 15) != 0) return false;
+    if ((reinterpret_cast<uintptr_t>(y) & 15u) != 0) return false;
     return rows * (row_bytes >> 4) >= kGatherFlatMinVectors;
 }
 
