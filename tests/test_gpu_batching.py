@@ -76,6 +76,8 @@ FUZZ = [
     (64, 64, 8, 4096, 8, 1, 1, "zipf", 0.05),          # 32768 slots: one-launch sort at 64 tiles
     (3, 10923, 1, 4097, 8, 0, 1, "uniform", 0.1),      # 32769 slots: past it, the kernel chain
     (4, 64, 9, 8192, 8, 1, 1, "zipf", 0.1),            # 2304 slots, 8193 keys: chain (key limit)
+    (64, 64, 64, 1, 8, 1, 1, "uniform", 0.0),          # 262144 slots of one key: 128 full tiles of it
+    (256, 64, 9, 1024, 8, 1, 4, "zipf", 0.05),         # the round trip's 147456 slots and 1025 keys
 ]
 
 
