@@ -217,7 +217,9 @@ mr_status ffnwb_batching_ex(const int32_t* expertIds, int32_t layerId, const voi
  *                    micro_batch_size * selected_expert_num i32 expert ids.
  *                    token_data_buf holds one row per slot in the same order:
  *                    H values (FP16/BF16) or H int8 values and their fp32
- *                    scale (INT8, stride H + 4).
+ *                    scale (INT8, stride H + 4), at any alignment (FP16/BF16
+ *                    rows of whole 16-byte vectors at a 16-byte aligned
+ *                    address copy fastest; the kernel checks the address).
  *   Slot g of block b: session id b / micro_batch_num, micro-batch id
  *   b % micro_batch_num, token id g, key = layer_id(b) * E_l + id (masked if
  *   the id or the block's layer is out of range).
