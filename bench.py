@@ -62,7 +62,7 @@ def parse_args(argv=None):
     ap.add_argument("--small", action="store_true", help="a small case of the same workload (profiling)")
     ap.add_argument("--workload", choices=["roundtrip", "tiny", "topk", "int8", "padded", "context",
                                            "batching", "permute", "permute_padded", "update_expert", "decode_unpermute",
-                                           "padded_slack"],
+                                           "padded_slack", "batching_index", "large_map", "odd_h", "padded_lsd"],
                     default="roundtrip",
                     help="roundtrip (the bench line) or one of the other workloads, timed per call "
                          "with an L2 flush before each")
@@ -654,11 +654,12 @@ def run_workload(args):
             out = usc.moe_update_expert(ids, tab, local_rank=3, world_size=u["world_size"], balance_mode=0,
                                         scales=sc, threshold=thr, active=act, out=out)
         phases = (0,)
-    elif name in ("context", "batching"):
+    elif name in ("context", "batching", "batching_index"):
         # the round trip's batching alone, from flat arrays or from a
         # ScheduleContext (256 sessions x 4 micro-batches x 16 tokens x 9;
-        # --small: 32 sessions, for profiling)
-        spec = dict(w.ROUNDTRIP_BATCHING)
+        # --small: 32 sessions, for profiling); batching_index: its slots and
+        # keys with 16-byte rows
+        spec = dict(w.ROUNDTRIP_BATCHING_INDEX if name == "batching_index" else w.ROUNDTRIP_BATCHING)
         if args.small:
             spec.update(A=32, session=32)
         inp = w.make_batching(**spec)
@@ -728,6 +729,12 @@ def run_workload(args):
             u = w.make_unpermute_topk(**w.UNPERMUTE_DECODE)
         elif name == "padded_slack":
             u = w.make_unpermute_padded(**w.UNPERMUTE_PADDED_SLACK)
+        elif name == "large_map":
+            u = w.make_unpermute_topk(**w.UNPERMUTE_LARGE_MAP)
+        elif name == "odd_h":
+            u = w.make_unpermute_topk(**w.UNPERMUTE_ODD_H)
+        elif name == "padded_lsd":
+            u = w.make_unpermute_padded(**w.UNPERMUTE_PADDED_LSD)
         else:
             u = w.make_unpermute_padded(**w.UNPERMUTE_PADDED)
         T, H, n, dt, pdt, Eu = u["T"], u["H"], u["n"], u["tokenDtype"], u["probsDtype"], u["Eu"]

@@ -71,15 +71,29 @@ def assert_batching_equal(got, ref, with_sorted=True):
                               ref["dynamicScale"][:U].view(np.uint32))
 
 
-def run_unpermute(inp, *, stream=None, workspace=None, out=None, pass_restore=None):
+def offset_dev(a, offset):
+    """A device copy of `a` starting `offset` bytes into its allocation."""
+    raw = np.ascontiguousarray(a)
+    buf = torch.zeros(raw.nbytes + offset, dtype=torch.uint8, device="cuda")
+    buf[offset:] = torch.from_numpy(raw.view(np.uint8).reshape(-1)).cuda()
+    return buf[offset:].view(TORCH_RAW[raw.dtype]).view(*raw.shape)
+
+
+TORCH_RAW = {np.dtype(np.int8): torch.int8, np.dtype(np.uint8): torch.uint8}
+
+
+def run_unpermute(inp, *, stream=None, workspace=None, out=None, pass_restore=None, map_offset=0):
     probs = inp.get("probs")
     dt, pdt = inp["tokenDtype"], inp["probsDtype"]
     rs = None
     if probs is None or pass_restore:
         rs = (inp["T"], inp["H"])
+    rmap = None
+    if probs is not None:
+        rmap = offset_dev(inp["routingMap"], map_offset) if map_offset else to_dev(inp["routingMap"])
     res = usc.moe_unpermute(
         float_tensor(inp["permuted"], dt), to_dev(inp["sortedIndices"]),
-        to_dev(inp["routingMap"]) if probs is not None else None,
+        rmap,
         float_tensor(probs, pdt) if probs is not None else None,
         padded_mode=bool(inp["padded"]), restore_shape=rs, stream=stream, workspace=workspace,
         out=out)

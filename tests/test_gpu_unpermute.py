@@ -130,6 +130,20 @@ def test_more_routing_ones_than_slots(T, Eu):
     check(inp)
 
 
+@pytest.mark.parametrize("Eu,off", [(67, 0), (64, 1), (64, 4)])
+def test_large_map_layouts(Eu, off):
+    """Routing maps past the one-kernel maskedSelect (more than 4M entries):
+    an expert count that is not a multiple of 4 (column masks one expert per
+    lane; the scatter's 16-entry loads cross token rows), and maps 1 and 4
+    bytes past a 16-byte boundary (the byte and 4-byte forms)."""
+    T = (1 << 22) // Eu + 64
+    inp = w.make_unpermute_topk(T=T, k=4, Eu=Eu, H=8, dtype=1, probs_dtype=1, choices=(1, 4), seed=Eu + off)
+    assert T * Eu > (1 << 22)
+    ref = oracle.unpermute(inp)
+    got = unpermute_numpy(run_unpermute(inp, map_offset=off), inp)
+    assert_unpermute_equal(got, ref, inp)
+
+
 @pytest.mark.parametrize("rows_extra", [0, 5])
 def test_no_probs_restore_shape(rows_extra):
     """Branches (3)/(4) take the token count from restoreShape."""

@@ -93,7 +93,7 @@ extern "C" mr_status ffnwb_batching_ex(const int32_t* expertIds, int32_t layerId
     const uint8_t* sp = reinterpret_cast<const uint8_t*>(scales);
     uint8_t* yb = reinterpret_cast<uint8_t*>(y);
     if (gather_flat_ok(tokenData, tokenRowStride, p.row_bytes, y, int8 ? scales : nullptr, scaleStride, p.Y)) {
-        MR_TRY_CUDA(launch_pdl(batching_gather_flat_kernel, dim3(gather_flat_grid(p.Y, p.row_bytes)),
+        MR_TRY_CUDA(launch_pdl(gather_flat_kernel_for(p.row_bytes), dim3(gather_flat_grid(p.Y, p.row_bytes)),
                                dim3(kGatherThreads), 0, s, td, tokenRowStride, p.row_bytes, int8 ? 1 : 0, sp,
                                scaleStride, yb, dynamicScale, (const int32_t*)gather_idx,
                                (const uint32_t*)cs.bucket_start, row_keys, (const uint64_t*)nullptr, p.Y));

@@ -225,7 +225,7 @@ extern "C" mr_status ffnwb_batching_context_ex(
     const uint64_t* td_loc = reinterpret_cast<const uint64_t*>(ctx + kCtxTokenDataField);
     uint8_t* yb = reinterpret_cast<uint8_t*>(y);
     if (!int8 && gather_flat_ok_device_base(row_stride, p.row_bytes, y, p.Y)) {
-        MR_TRY_CUDA(launch_pdl(batching_gather_flat_kernel, dim3(gather_flat_grid(p.Y, p.row_bytes)),
+        MR_TRY_CUDA(launch_pdl(gather_flat_kernel_for(p.row_bytes), dim3(gather_flat_grid(p.Y, p.row_bytes)),
                                dim3(kGatherThreads), 0, s, (const uint8_t*)nullptr, row_stride, p.row_bytes, 0,
                                (const uint8_t*)nullptr, (int64_t)4, yb, dynamicScale,
                                (const int32_t*)gather_idx, (const uint32_t*)cs.bucket_start, row_keys, td_loc,

@@ -210,6 +210,8 @@ static __device__ __noinline__ void gather_flat_unaligned(
     }
 }
 
+// SHORT: rows of fewer than kGatherThreads vectors.
+template <bool SHORT>
 static __global__ void __launch_bounds__(kGatherThreads, 6)
 batching_gather_flat_kernel(const uint8_t* __restrict__ token_data_arg, int64_t row_stride, int64_t row_bytes,
                             int is_int8, const uint8_t* __restrict__ scales, int64_t scale_stride,
@@ -251,10 +253,19 @@ batching_gather_flat_kernel(const uint8_t* __restrict__ token_data_arg, int64_t 
                 }
             }
             // the next vector of this thread: kGatherThreads vectors further on
+            // (rows of at least kGatherThreads vectors: at most one row
+            // boundary per step; SHORT rows: a division, not up to
+            // kGatherThreads subtractions)
             o += kGatherThreads;
-            while (o >= nvec) {
-                o -= nvec;
-                ++row;
+            if (!SHORT) {
+                while (o >= nvec) {
+                    o -= nvec;
+                    ++row;
+                }
+            } else if (o >= nvec) {
+                const int q = (int)o / (int)nvec;
+                row += q;
+                o -= (int64_t)q * nvec;
             }
         }
 #pragma unroll
@@ -284,6 +295,12 @@ inline bool gather_flat_ok_device_base(int64_t row_stride, int64_t row_bytes, co
     if ((row_bytes & 15) != 0 || (row_stride & 15) != 0) return false;
     if ((reinterpret_cast<uintptr_t>(y) & 15u) != 0) return false;
     return rows * (row_bytes >> 4) >= kGatherFlatMinVectors;
+}
+
+// The flat gather's instantiation for rows of row_bytes.
+inline auto gather_flat_kernel_for(int64_t row_bytes) {
+    return (row_bytes >> 4) < kGatherThreads ? batching_gather_flat_kernel<true>
+                                             : batching_gather_flat_kernel<false>;
 }
 
 // Blocks of the flat gather for up to `rows` output rows (every vector of

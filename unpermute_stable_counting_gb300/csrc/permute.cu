@@ -293,12 +293,8 @@ extern "C" mr_status moe_permute(const void* tokens, const int8_t* routingMap, i
     q += align_up((uint64_t)(p.Eu + 1) * 4u, 256);
     uint32_t* ticket = reinterpret_cast<uint32_t*>(q);
 
-    const int64_t mgrid_want = (p.nblk * ((p.Eu + 31) / 32) * 32 + 255) / 256;
-    const int64_t mgrid_cap = (int64_t)device_sm_count() * 8;
-    const int mgrid = (int)(mgrid_want < mgrid_cap ? (mgrid_want > 0 ? mgrid_want : 1) : mgrid_cap);
     profile_mark(s, 0);
-    MR_TRY_CUDA(launch_pdl(mask_columns_kernel, dim3(mgrid), dim3(256), 0, s, routingMap, p.T, p.Eu,
-                           masks, offs, ticket));
+    MR_TRY_CUDA(launch_mask_columns(routingMap, p.T, p.Eu, masks, offs, ticket, s));
     GroupListOut none{nullptr, nullptr, 0};
     MR_TRY_CUDA(csort_prefix(offs, p.nblk, (int)p.Eu, totals, bstart, ticket, none, s));
     profile_mark(s, 1);

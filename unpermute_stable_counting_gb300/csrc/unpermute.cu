@@ -42,8 +42,22 @@
 namespace mr {
 namespace cg = cooperative_groups;
 
-// One thread per (token, expert) element: a routed element lands at
-// bucket_start[e] + offs[blk][e] + (routed tokens of its block below it).
+// maskedSelect beyond the one-kernel form's limit: a routed (token, expert)
+// element lands at bucket_start[e] + offs[blk][e] + (routed tokens of its
+// block below it).
+__device__ __forceinline__ void mask_scatter_one(const uint32_t* __restrict__ masks,
+                                                 const uint32_t* __restrict__ offs,
+                                                 const uint32_t* __restrict__ bucket_start, int64_t Eu,
+                                                 int64_t n, const uint8_t* __restrict__ probs, int pes,
+                                                 uint8_t* __restrict__ pp, int64_t i, int64_t t, int64_t e) {
+    const int64_t item = (t >> 5) * Eu + e;
+    const uint32_t below = masks[item] & ((1u << (t & 31)) - 1u);
+    const int64_t pos = (int64_t)bucket_start[e] + offs[item] + __popc(below);
+    if (pos < n) copy_prob(pp, pos, probs, i, pes);
+}
+
+// The map is read 16 entries per thread (one 16-byte load; most entries are
+// 0 and cost nothing more) when it is 16-byte aligned, the rest one by one.
 __global__ void __launch_bounds__(256)
 mask_scatter_kernel(const int8_t* __restrict__ map, const uint32_t* __restrict__ masks,
                     const uint32_t* __restrict__ offs, const uint32_t* __restrict__ bucket_start,
@@ -53,18 +67,31 @@ mask_scatter_kernel(const int8_t* __restrict__ map, const uint32_t* __restrict__
     const int64_t N = T * Eu;
     const int64_t nnz = bucket_start[Eu];
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
-    const int64_t total = N > n ? N : n;
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += stride) {
-        if (i < N && map[i] != 0) {
-            const int64_t t = i / Eu;
-            const int64_t e = i - t * Eu;
-            const int64_t item = (t >> 5) * Eu + e;
-            const uint32_t below = masks[item] & ((1u << (t & 31)) - 1u);
-            const int64_t pos = (int64_t)bucket_start[e] + offs[item] + __popc(below);
-            if (pos < n) copy_prob(pp, pos, probs, i, pes);
+    const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t nv = (reinterpret_cast<uintptr_t>(map) & 15u) == 0u ? N / 16 : 0;
+    for (int64_t v = tid; v < nv; v += stride) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4*>(map) + v);
+        if ((w.x | w.y | w.z | w.w) == 0u) continue;
+        const uint32_t word[4] = {w.x, w.y, w.z, w.w};
+        const int64_t i0 = v * 16;
+        int64_t t = i0 / Eu, e = i0 - t * Eu;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (((word[k >> 2] >> (8 * (k & 3))) & 0xffu) != 0u)
+                mask_scatter_one(masks, offs, bucket_start, Eu, n, probs, pes, pp, i0 + k, t, e);
+            if (++e == Eu) {
+                e = 0;
+                ++t;
+            }
         }
-        if (i >= nnz && i < n) zero_prob(pp, i, pes);
     }
+    for (int64_t i = nv * 16 + tid; i < N; i += stride) {
+        if (map[i] != 0) {
+            const int64_t t = i / Eu;
+            mask_scatter_one(masks, offs, bucket_start, Eu, n, probs, pes, pp, i, t, i - t * Eu);
+        }
+    }
+    for (int64_t i = nnz + tid; i < n; i += stride) zero_prob(pp, i, pes);
 }
 
 // One-kernel maskedSelect (not padded, with probs) for maps of at most
@@ -646,8 +673,7 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
         uint32_t* bstart = reinterpret_cast<uint32_t*>(q);
         q += align_up((uint64_t)(p.Eu + 1) * 4u, 256);
         uint32_t* ticket = reinterpret_cast<uint32_t*>(q);
-        cudaError_t e = launch_pdl(mask_columns_kernel, dim3(elementwise_grid(nblk * ((p.Eu + 31) / 32) * 32)),
-                                   dim3(256), 0, ss, routingMap, p.T, p.Eu, masks, offs, ticket);
+        cudaError_t e = launch_mask_columns(routingMap, p.T, p.Eu, masks, offs, ticket, ss);
         if (e != cudaSuccess) return e;
         GroupListOut none{nullptr, nullptr, 0};
         e = csort_prefix(offs, nblk, (int)p.Eu, totals, bstart, ticket, none, ss);

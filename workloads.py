@@ -183,11 +183,10 @@ def make_unpermute_topk(*, T: int, k: int, Eu: int, H: int, dtype: int, probs_dt
     row_of_pair = np.empty(len(tt), dtype=np.int64)
     row_of_pair[pair_order] = np.arange(len(tt))
     sorted_idx = np.full(T * k, -1, dtype=np.int32)
-    slot = np.zeros(T, dtype=np.int64)
-    for p in range(len(tt)):                       # pairs of a token come in ascending expert id
-        t = tt[p]
-        sorted_idx[t * k + slot[t]] = row_of_pair[p]
-        slot[t] += 1
+    # a token's pairs come in ascending expert id: slot j of the token is its
+    # j-th pair
+    j = np.arange(len(tt)) - np.searchsorted(tt, tt)
+    sorted_idx[tt * k + j] = row_of_pair
     nrows = T * k if rows is None else rows
     permuted = normal_rows(nrows, H, dtype, seed)
     probs = None
@@ -264,6 +263,16 @@ ROUNDTRIP_BATCHING = dict(A=256, BS=64, K1=9, E=1024, H=7168, dtype=DT_BF16, lay
                           layer_id=2, ids="zipf", zipf_s=1.2, mask=0.05, session=256, micro=64,
                           token_ids=True, seed=4)
 ROUNDTRIP_PROBS_DTYPE = DT_BF16
+
+# Shapes that take the library's other paths, for measuring those kernels:
+# the round trip's slots and keys with 16-byte rows (its index kernels alone);
+# a routing map of more than 4M entries (the three-kernel maskedSelect); rows
+# that are not whole 16-byte vectors (the element-wise gather-reduce); and a
+# padded sort of more than 2^22 keys (LSD passes, then the row pointers).
+ROUNDTRIP_BATCHING_INDEX = dict(ROUNDTRIP_BATCHING, H=8)
+UNPERMUTE_LARGE_MAP = dict(T=32768, k=8, Eu=256, H=512, dtype=DT_BF16, probs_dtype=DT_BF16, seed=8)
+UNPERMUTE_ODD_H = dict(UNPERMUTE_TOPK, H=4095)
+UNPERMUTE_PADDED_LSD = dict(T=1 << 22, Eu=2, k=1, H=8, dtype=DT_F16, probs_dtype=DT_F32, seed=9)
 
 
 # ---------------------------------------------------------------------------
