@@ -42,53 +42,31 @@
 namespace mr {
 namespace cg = cooperative_groups;
 
-// maskedSelect beyond the one-kernel form's limit: a routed (token, expert)
-// element lands at bucket_start[e] + offs[blk][e] + (routed tokens of its
-// block below it).
-__device__ __forceinline__ void mask_scatter_one(const uint32_t* __restrict__ masks,
-                                                 const uint32_t* __restrict__ offs,
-                                                 const uint32_t* __restrict__ bucket_start, int64_t Eu,
-                                                 int64_t n, const uint8_t* __restrict__ probs, int pes,
-                                                 uint8_t* __restrict__ pp, int64_t i, int64_t t, int64_t e) {
-    const int64_t item = (t >> 5) * Eu + e;
-    const uint32_t below = masks[item] & ((1u << (t & 31)) - 1u);
-    const int64_t pos = (int64_t)bucket_start[e] + offs[item] + __popc(below);
-    if (pos < n) copy_prob(pp, pos, probs, i, pes);
-}
-
-// The map is read 16 entries per thread (one 16-byte load; most entries are
-// 0 and cost nothing more) when it is 16-byte aligned, the rest one by one.
+// maskedSelect beyond the one-kernel form's limit, from the column masks:
+// one thread per (32-token block, expert) item; the routed tokens of the
+// item's mask land at bucket_start[e] + offs[blk][e] + (set bits below
+// them). Threads of consecutive experts read consecutive mask, offset and
+// probs words; the routing map itself is not read again.
 __global__ void __launch_bounds__(256)
-mask_scatter_kernel(const int8_t* __restrict__ map, const uint32_t* __restrict__ masks,
-                    const uint32_t* __restrict__ offs, const uint32_t* __restrict__ bucket_start,
-                    int64_t T, int64_t Eu, int64_t n, const uint8_t* __restrict__ probs, int pes,
-                    uint8_t* __restrict__ pp) {
+mask_scatter_kernel(const uint32_t* __restrict__ masks, const uint32_t* __restrict__ offs,
+                    const uint32_t* __restrict__ bucket_start, int64_t T, int64_t Eu, int64_t n,
+                    const uint8_t* __restrict__ probs, int pes, uint8_t* __restrict__ pp) {
     pdl_enter();
-    const int64_t N = T * Eu;
+    const int64_t items = (T + 31) / 32 * Eu;
     const int64_t nnz = bucket_start[Eu];
     const int64_t stride = (int64_t)gridDim.x * blockDim.x;
     const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    const int64_t nv = (reinterpret_cast<uintptr_t>(map) & 15u) == 0u ? N / 16 : 0;
-    for (int64_t v = tid; v < nv; v += stride) {
-        const uint4 w = __ldg(reinterpret_cast<const uint4*>(map) + v);
-        if ((w.x | w.y | w.z | w.w) == 0u) continue;
-        const uint32_t word[4] = {w.x, w.y, w.z, w.w};
-        const int64_t i0 = v * 16;
-        int64_t t = i0 / Eu, e = i0 - t * Eu;
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            if (((word[k >> 2] >> (8 * (k & 3))) & 0xffu) != 0u)
-                mask_scatter_one(masks, offs, bucket_start, Eu, n, probs, pes, pp, i0 + k, t, e);
-            if (++e == Eu) {
-                e = 0;
-                ++t;
-            }
-        }
-    }
-    for (int64_t i = nv * 16 + tid; i < N; i += stride) {
-        if (map[i] != 0) {
-            const int64_t t = i / Eu;
-            mask_scatter_one(masks, offs, bucket_start, Eu, n, probs, pes, pp, i, t, i - t * Eu);
+    for (int64_t item = tid; item < items; item += stride) {
+        uint32_t bits = masks[item];
+        if (bits == 0u) continue;
+        const int64_t blk = item / Eu;
+        const int64_t e = item - blk * Eu;
+        int64_t pos = (int64_t)bucket_start[e] + offs[item];
+        while (bits) {
+            const int j = __ffs(bits) - 1;
+            bits &= bits - 1u;
+            if (pos < n) copy_prob(pp, pos, probs, (blk * 32 + j) * Eu + e, pes);
+            ++pos;
         }
     }
     for (int64_t i = nnz + tid; i < n; i += stride) zero_prob(pp, i, pes);
@@ -678,8 +656,8 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
         GroupListOut none{nullptr, nullptr, 0};
         e = csort_prefix(offs, nblk, (int)p.Eu, totals, bstart, ticket, none, ss);
         if (e != cudaSuccess) return e;
-        const int64_t work = p.T * p.Eu > p.n ? p.T * p.Eu : p.n;
-        return launch_pdl(mask_scatter_kernel, dim3(elementwise_grid(work)), dim3(256), 0, ss, routingMap,
+        const int64_t work = items > p.n ? items : p.n;
+        return launch_pdl(mask_scatter_kernel, dim3(elementwise_grid(work)), dim3(256), 0, ss,
                           (const uint32_t*)masks, (const uint32_t*)offs, (const uint32_t*)bstart, p.T, p.Eu,
                           p.n, reinterpret_cast<const uint8_t*>(probs), p.pes, pp);
     };
