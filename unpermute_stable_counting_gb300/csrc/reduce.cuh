@@ -386,7 +386,10 @@ unpermute_reduce_warp_kernel(const uint8_t* __restrict__ permuted, int64_t rows,
 
 // Element-wise variant for rows that are not 16-byte vectors (odd H or
 // buffers not 16-byte aligned; element alignment is required). Same list,
-// same order, same arithmetic.
+// same order, same arithmetic. One block per token; its list is built once
+// (up to kListCap slots) and each thread adds kScalarPer elements at a time
+// (their row loads issued together).
+constexpr int kScalarPer = 4;
 template <int TDT, int PDT, bool HAS_PROBS, bool PADDED>
 __global__ void __launch_bounds__(256)
 unpermute_reduce_scalar_kernel(const uint8_t* __restrict__ permuted, int64_t rows, int64_t H,
@@ -411,41 +414,68 @@ unpermute_reduce_scalar_kernel(const uint8_t* __restrict__ permuted, int64_t row
             L0 = t * topk;
             L1 = L0 + topk;
         }
-        for (int64_t h0 = 0; h0 < H; h0 += blockDim.x) {
-            const int64_t h = h0 + threadIdx.x;
-            float acc = 0.0f;
+        // a list of at most kListCap slots is built once for every hidden
+        // step of the token; a longer one a part at a time, in each step
+        const bool one_list = L1 - L0 <= kListCap;
+        if (one_list && L1 > L0) {
+            if (threadIdx.x < 32) {
+                const int cnt = build_list<HAS_PROBS, PADDED, PDT>(L0, L1, si, rows, row_bytes, pp,
+                                                                   out_index, s_row, s_w);
+                if (threadIdx.x == 0) s_cnt = cnt;
+            }
+            __syncthreads();
+        }
+        // each thread adds kScalarPer elements, blockDim.x apart, at a time
+        for (int64_t h0 = 0; h0 < H; h0 += (int64_t)blockDim.x * kScalarPer) {
+            float acc[kScalarPer];
+#pragma unroll
+            for (int k = 0; k < kScalarPer; ++k) acc[k] = 0.0f;
             for (int64_t c0 = L0; c0 < L1; c0 += kListCap) {
                 const int64_t c1 = c0 + kListCap < L1 ? c0 + kListCap : L1;
-                if (threadIdx.x < 32) {
-                    const int cnt = build_list<HAS_PROBS, PADDED, PDT>(c0, c1, si, rows, row_bytes,
-                                                                       pp, out_index, s_row, s_w);
-                    if (threadIdx.x == 0) s_cnt = cnt;
-                }
-                __syncthreads();
-                const int cnt = s_cnt;
-                if (h < H) {
-                    for (int m = 0; m < cnt; ++m) {
-                        const uint8_t* rp = permuted + s_row[m] + h * es;
-                        float x;
-                        if constexpr (TDT == MR_DTYPE_F32) {
-                            x = __ldg(reinterpret_cast<const float*>(rp));
-                        } else {
-                            x = Elem<TDT>::to_f32(__ldg(reinterpret_cast<const unsigned short*>(rp)));
-                        }
-                        acc = HAS_PROBS ? __fadd_rn(acc, __fmul_rn(x, s_w[m])) : __fadd_rn(acc, x);
+                if (!one_list) {
+                    if (threadIdx.x < 32) {
+                        const int cnt = build_list<HAS_PROBS, PADDED, PDT>(c0, c1, si, rows, row_bytes,
+                                                                           pp, out_index, s_row, s_w);
+                        if (threadIdx.x == 0) s_cnt = cnt;
                     }
+                    __syncthreads();
                 }
-                __syncthreads();
+                const int cnt = s_cnt;
+                for (int m = 0; m < cnt; ++m) {
+                    const uint8_t* rp = permuted + s_row[m];
+                    float x[kScalarPer];
+#pragma unroll
+                    for (int k = 0; k < kScalarPer; ++k) {
+                        const int64_t h = h0 + threadIdx.x + (int64_t)k * blockDim.x;
+                        x[k] = 0.0f;
+                        if (h < H) {
+                            if constexpr (TDT == MR_DTYPE_F32) {
+                                x[k] = __ldg(reinterpret_cast<const float*>(rp + h * es));
+                            } else {
+                                x[k] = Elem<TDT>::to_f32(__ldg(reinterpret_cast<const unsigned short*>(rp + h * es)));
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < kScalarPer; ++k)
+                        acc[k] = HAS_PROBS ? __fadd_rn(acc[k], __fmul_rn(x[k], s_w[m])) : __fadd_rn(acc[k], x[k]);
+                }
+                if (!one_list) __syncthreads();  // the next part overwrites the list
             }
-            if (h < H) {
-                uint8_t* op = out + t * row_bytes + h * es;
-                if constexpr (TDT == MR_DTYPE_F32) {
-                    *reinterpret_cast<float*>(op) = acc;
-                } else {
-                    *reinterpret_cast<uint16_t*>(op) = Elem<TDT>::from_f32(acc);
+#pragma unroll
+            for (int k = 0; k < kScalarPer; ++k) {
+                const int64_t h = h0 + threadIdx.x + (int64_t)k * blockDim.x;
+                if (h < H) {
+                    uint8_t* op = out + t * row_bytes + h * es;
+                    if constexpr (TDT == MR_DTYPE_F32) {
+                        *reinterpret_cast<float*>(op) = acc[k];
+                    } else {
+                        *reinterpret_cast<uint16_t*>(op) = Elem<TDT>::from_f32(acc[k]);
+                    }
                 }
             }
         }
+        if (one_list && L1 > L0) __syncthreads();  // the next token's list overwrites it
     }
 }
 
