@@ -100,14 +100,17 @@ def test_random_contexts(dtype, layers, L, seed):
     run_both(ctx_d, host, (sessions + 2, micro * mbs, sel, H), E, dtype, 0, layerNum=L)
 
 
-@pytest.mark.parametrize("dtype,off", [(1, 0), (1, 2), (1, 4), (1, 8), (0, 12), (2, 0), (2, 4)])
-def test_token_buffer_alignment(dtype, off):
-    # 16-bit rows of 8 KB over 1152 slots take the flat gather, whose source
-    # address is read on the device and checked there: an aligned base, and
-    # bases 2 to 12 bytes past a 16-byte boundary (the word and byte forms);
-    # INT8 rows with their scale stay with the warp kernel
-    sessions, micro, mbs, sel, H = 4, 2, 16, 9, 4096
-    rng = np.random.default_rng(40 + off)
+@pytest.mark.parametrize("dtype,off,H,sessions", [(1, 0, 4096, 4), (1, 2, 4096, 4), (1, 4, 4096, 4),
+                                                   (1, 8, 4096, 4), (0, 12, 4096, 4), (2, 0, 4096, 4),
+                                                   (2, 4, 4096, 4), (1, 0, 64, 32), (0, 6, 64, 32)])
+def test_token_buffer_alignment(dtype, off, H, sessions):
+    # 16-bit rows take the flat gather (rows of 8 KB over 1152 slots; rows of
+    # 128 bytes over 9216 slots, its short-row form), whose source address is
+    # read on the device and checked there: an aligned base, and bases 2 to 12
+    # bytes past a 16-byte boundary (the word and byte forms); INT8 rows with
+    # their scale stay with the warp kernel
+    micro, mbs, sel = 2, 16, 9
+    rng = np.random.default_rng(40 + off + H)
     slots = sessions * micro * mbs * sel
     ids = rng.integers(-1, 66, size=slots).astype(np.int32)
     ctx_d, host, keep = device_context(sessions=sessions, micro=micro, mbs=mbs, sel=sel, E=64, H=H,
