@@ -8,7 +8,8 @@
 //   not padded, probs : maskedSelect: one cooperative kernel (counts per
 //                       tile, a grid barrier, the scatter and zero tail) up
 //                       to 4096 tiles of 1024 map entries, else column
-//                       bitmasks -> csort prefix -> scatter; for a small
+//                       bitmasks -> csort prefix -> scatter from the
+//                       bitmasks; for a small
 //                       routing map the gather-reduce selects the weights
 //                       itself instead
 //   always            : stable sort of sortedIndices -> outIndex,
@@ -20,9 +21,9 @@
 //                       the sorted keys
 //   padded, probs     : permuteProbs[i] = probs[sortedIndices[i], i // capacity],
 //                       written by the sort's first scatter
-//   not padded        : the sort runs on the library's auxiliary stream,
-//                       overlapping the maskedSelect and the gather-reduce
-//                       (fork/join events)
+//   not padded        : the sort runs on the caller stream's auxiliary
+//                       stream, overlapping the maskedSelect and the
+//                       gather-reduce (fork/join events)
 //   always            : gather-reduce (reduce.cuh), one warp per (token, run
 //                       of hidden chunks), fp32 accumulation in ascending slot
 //                       / row order, atomic-free, one RNE cast per output
