@@ -217,7 +217,7 @@ mask_select_kernel(const int8_t* __restrict__ map, int64_t T, int64_t Eu, int64_
 // ---------------------------------------------------------------------------
 
 constexpr int kRadixDigitBits = 12;
-constexpr double kPdlReduceBytes = 1e9;  // see the not-padded launch below
+constexpr double kShortReduceBytes = 1e9;  // see the not-padded launch below
 constexpr int64_t kSortReserveSMs = 8;    // SMs a short reduce leaves to the concurrent sort
 
 struct UnpermutePlan {
@@ -388,7 +388,7 @@ template <int TDT, int PDT, bool HAS_PROBS, bool PADDED, bool SMALL>
 static cudaError_t launch_reduce_vec(const UnpermutePlan& p, const uint8_t* permuted,
                                      const int32_t* si, const void* pp, const int32_t* out_index,
                                      const int32_t* ptr, uint8_t* out, const SmallMap& smap,
-                                     cudaStream_t s, bool pdl) {
+                                     cudaStream_t s, bool short_grid) {
     const int64_t row_bytes = p.H * p.es;
     const int64_t nvec = row_bytes / 16;
     const int64_t chunks = (nvec + 32 * kRedVQ - 1) / (32 * kRedVQ);
@@ -417,12 +417,12 @@ static cudaError_t launch_reduce_vec(const UnpermutePlan& p, const uint8_t* perm
     const int64_t long_units = p.T * ((chunks + kRedRun - 1) / kRedRun);
     auto kern = long_units < cap * 8 ? unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED, 1, SMALL>
                                      : unpermute_reduce_warp_kernel<TDT, PDT, HAS_PROBS, PADDED, kRedRun, SMALL>;
-    if (!pdl) {
-        // A short reduce launched in plain order has the index sort running
-        // beside it on the (higher-priority) auxiliary stream. Its grid is one
-        // work unit per warp (blocks retire as they finish and the sort's
-        // blocks take the freed slots), capped at a persistent grid on all
-        // SMs but kSortReserveSMs, so that the sort also has SMs of its own
+    if (short_grid) {
+        // A short reduce has the index sort running beside it on the
+        // (higher-priority) auxiliary stream. Its grid is one work unit per
+        // warp (blocks retire as they finish and the sort's blocks take the
+        // freed slots), capped at a persistent grid on all SMs but
+        // kSortReserveSMs, so that the sort also has SMs of its own
         // (measured on GB300, top-k T=4096, k=8, H=4096: a persistent grid on
         // every SM 55.6 us, one unit per warp 53.5 us, with the cap 51.5 us;
         // a decode step's few units stay below the cap)
@@ -435,42 +435,42 @@ static cudaError_t launch_reduce_vec(const UnpermutePlan& p, const uint8_t* perm
         if (grid > 0x7fffffff) grid = 0x7fffffff;
         if (grid < 1) grid = 1;
     }
-    return launch_kernel(pdl, kern, dim3((unsigned)grid), dim3(256), smem, s, permuted, p.rows, row_bytes,
-                         nvec, chunks, si, p.topk, pp, out_index, ptr, p.T, out, smap);
+    return launch_pdl(kern, dim3((unsigned)grid), dim3(256), smem, s, permuted, p.rows, row_bytes, nvec, chunks,
+                      si, p.topk, pp, out_index, ptr, p.T, out, smap);
 }
 
 template <int TDT, int PDT, bool HAS_PROBS, bool PADDED>
 static cudaError_t launch_reduce(const UnpermutePlan& p, const uint8_t* permuted,
                                  const int32_t* si, const void* pp, const int32_t* out_index,
                                  const int32_t* ptr, uint8_t* out, const SmallMap& smap,
-                                 cudaStream_t s, bool pdl) {
+                                 cudaStream_t s, bool short_grid) {
     if (reduce_vec_ok(p, permuted, out)) {
         if constexpr (HAS_PROBS && !PADDED) {
             if (smap.map)
                 return launch_reduce_vec<TDT, PDT, HAS_PROBS, PADDED, true>(p, permuted, si, pp, out_index,
-                                                                           ptr, out, smap, s, pdl);
+                                                                           ptr, out, smap, s, short_grid);
         }
         return launch_reduce_vec<TDT, PDT, HAS_PROBS, PADDED, false>(p, permuted, si, pp, out_index, ptr,
-                                                                    out, smap, s, pdl);
+                                                                    out, smap, s, short_grid);
     }
     int64_t threads = p.H < 256 ? (p.H + 31) / 32 * 32 : 256;
     const int64_t gx = p.T < 0x7fffffff ? p.T : 0x7fffffff;
-    return launch_kernel(pdl, unpermute_reduce_scalar_kernel<TDT, PDT, HAS_PROBS, PADDED>, dim3((unsigned)gx),
-                      dim3((unsigned)threads), 0, s, permuted, p.rows, p.H, si, p.topk, pp,
-                      out_index, ptr, p.T, out);
+    return launch_pdl(unpermute_reduce_scalar_kernel<TDT, PDT, HAS_PROBS, PADDED>, dim3((unsigned)gx),
+                      dim3((unsigned)threads), 0, s, permuted, p.rows, p.H, si, p.topk, pp, out_index, ptr, p.T,
+                      out);
 }
 
 template <int TDT, int PDT>
 static cudaError_t dispatch_reduce(const UnpermutePlan& p, const uint8_t* permuted,
                                    const int32_t* si, const void* pp, const int32_t* out_index,
                                    const int32_t* ptr, uint8_t* out, const SmallMap& smap,
-                                   cudaStream_t s, bool pdl) {
+                                   cudaStream_t s, bool short_grid) {
     if (p.probs) {
-        return p.padded ? launch_reduce<TDT, PDT, true, true>(p, permuted, si, pp, out_index, ptr, out, smap, s, pdl)
-                        : launch_reduce<TDT, PDT, true, false>(p, permuted, si, pp, out_index, ptr, out, smap, s, pdl);
+        return p.padded ? launch_reduce<TDT, PDT, true, true>(p, permuted, si, pp, out_index, ptr, out, smap, s, short_grid)
+                        : launch_reduce<TDT, PDT, true, false>(p, permuted, si, pp, out_index, ptr, out, smap, s, short_grid);
     }
-    return p.padded ? launch_reduce<TDT, PDT, false, true>(p, permuted, si, pp, out_index, ptr, out, smap, s, pdl)
-                    : launch_reduce<TDT, PDT, false, false>(p, permuted, si, pp, out_index, ptr, out, smap, s, pdl);
+    return p.padded ? launch_reduce<TDT, PDT, false, true>(p, permuted, si, pp, out_index, ptr, out, smap, s, short_grid)
+                    : launch_reduce<TDT, PDT, false, false>(p, permuted, si, pp, out_index, ptr, out, smap, s, short_grid);
 }
 
 // The one-kernel maskedSelect: a cooperative launch (every block resident for
@@ -666,18 +666,18 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
     // ---- gather-reduce --------------------------------------------------------
     const uint8_t* permuted = reinterpret_cast<const uint8_t*>(permutedTokens);
     uint8_t* out = reinterpret_cast<uint8_t*>(unpermutedTokens);
-    auto launch_reduce_any = [&](cudaStream_t ss, bool pdl) -> cudaError_t {
+    auto launch_reduce_any = [&](cudaStream_t ss, bool short_grid) -> cudaError_t {
         switch (p.tdt * 4 + p.pdt) {
             case MR_DTYPE_F16 * 4 + MR_DTYPE_F16:
-                return dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, pdl);
+                return dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, short_grid);
             case MR_DTYPE_F16 * 4 + MR_DTYPE_F32:
-                return dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, pdl);
+                return dispatch_reduce<MR_DTYPE_F16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, short_grid);
             case MR_DTYPE_BF16 * 4 + MR_DTYPE_BF16:
-                return dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_BF16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, pdl);
+                return dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_BF16>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, short_grid);
             case MR_DTYPE_BF16 * 4 + MR_DTYPE_F32:
-                return dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, pdl);
+                return dispatch_reduce<MR_DTYPE_BF16, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, short_grid);
             case MR_DTYPE_F32 * 4 + MR_DTYPE_F32:
-                return dispatch_reduce<MR_DTYPE_F32, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, pdl);
+                return dispatch_reduce<MR_DTYPE_F32, MR_DTYPE_F32>(p, permuted, sortedIndices, pp, outIndex, ptr, out, smap, ss, short_grid);
         }
         return cudaErrorInvalidValue;
     };
@@ -704,16 +704,17 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
         }
         if (e == cudaSuccess) {
             profile_mark(s, 6);
-            // Under PDL the persistent reduce takes the SMs while it waits for
-            // the probs, and the concurrent sort then runs on what is left.
-            // A short reduce would end up waiting for the sort at the join,
-            // so it is launched in plain stream order (with a non-persistent
-            // grid, see launch_reduce_vec); a long one (here more than 1 GB of
-            // rows, ~150 us) hides the sort either way and keeps the launch
-            // overlap (measured on GB300: top-k T=4096, k=8, H=4096 75.7 ->
-            // 55.6 us; the 2.1 GB round trip 0.989 vs 0.995 ms)
+            // A persistent reduce, launched early under PDL, takes the SMs
+            // while it waits for the probs, and the concurrent sort then runs
+            // on what is left; a short reduce would end up waiting for the
+            // sort at the join. So a short one (up to 1 GB of rows, ~150 us)
+            // gets a grid of one work unit per warp, whose blocks retire as
+            // they finish (see launch_reduce_vec); a long one hides the sort
+            // either way and keeps the persistent grid (measured on GB300:
+            // top-k T=4096, k=8, H=4096: persistent grid 75.7 us; one unit per
+            // warp launched in plain order 49.4 us, under PDL 47.4 us)
             const double reduce_bytes = (double)p.T * (double)p.topk * (double)p.H * p.es;
-            e = launch_reduce_any(s, reduce_bytes > kPdlReduceBytes);
+            e = launch_reduce_any(s, reduce_bytes <= kShortReduceBytes);
             profile_mark(s, 7);
         }
         const cudaError_t ew = ej == cudaSuccess ? cudaStreamWaitEvent(s, ax->join, 0) : ej;
@@ -725,7 +726,7 @@ extern "C" mr_status moe_unpermute(const void* permutedTokens, const int32_t* so
         MR_TRY_CUDA(launch_sort(s));
         profile_mark(s, 5);
         profile_mark(s, 6);
-        e = launch_reduce_any(s, true);
+        e = launch_reduce_any(s, false);
         MR_TRY_CUDA(e);
         profile_mark(s, 7);
     }
