@@ -118,6 +118,18 @@ def test_token_buffer_alignment(dtype, off, H, sessions):
     run_both(ctx_d, host, (sessions, micro * mbs, sel, H), 64, dtype, 0)
 
 
+@pytest.mark.parametrize("dtype,off", [(1, 0), (1, 6), (0, 2), (2, 0), (2, 4)])
+def test_small_context_one_block(dtype, off):
+    # 144 slots of 128-byte rows (INT8: 68 bytes): one block sorts, scatters
+    # and gathers the rows; token buffers aligned and not
+    sessions, micro, mbs, sel, H = 2, 1, 8, 9, 64
+    rng = np.random.default_rng(70 + off + dtype)
+    ids = rng.integers(-1, 10, size=sessions * micro * mbs * sel).astype(np.int32)
+    ctx_d, host, keep = device_context(sessions=sessions, micro=micro, mbs=mbs, sel=sel, E=8, H=H,
+                                       dtype=dtype, ids=ids, seed=off, base_offset=off)
+    run_both(ctx_d, host, (sessions + 1, micro * mbs, sel, H), 8, dtype, 0)
+
+
 def test_need_schedule_all_ready():
     ids = np.random.default_rng(5).integers(0, 32, size=4 * 2 * 8 * 3).astype(np.int32)
     ctx_d, host, keep = device_context(sessions=4, micro=2, mbs=8, sel=3, E=32, H=64, dtype=1, ids=ids)
