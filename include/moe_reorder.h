@@ -486,7 +486,7 @@ int32_t mr_version(void);
  *   stream, phases being: 0 batching index build, 1 batching row gather,
  *   2 unpermute probs work (maskedSelect or the padded lookup; padded: also
  *   the sort), 3 unpermute gather-reduce, 4 the not-padded sort, which runs
- *   on the library's auxiliary stream (its events are recorded there).
+ *   on the caller stream's auxiliary stream (its events are recorded there).
  *   Phases beyond `count/2` are not recorded.
  *   The setting is per host thread. Returns MR_OK or MR_ERR_PARAM_INVALID.
  */
