@@ -131,3 +131,23 @@ def test_reference_arm_size_follows_the_step_budget():
     part = bench.reference_attn(bench.parse_args(["--impl", "reference", "--steps", "200", "--warmup", "10"]))
     assert part < 256 and 210 * bench.ORACLE_STEP_S_FULL * part / 256 <= bench.REFERENCE_BUDGET_S
     assert bench.reference_attn(bench.parse_args(["--cpu-sample-attn", "2"])) == 2
+
+
+def test_other_path_workloads_reach_their_paths():
+    """The recipes of the bench's other-path workloads have the shapes that
+    take those paths: the batching kernel chain with short flat-gather rows,
+    the three-kernel maskedSelect (more than 4M routing-map entries), the
+    element-wise gather-reduce (rows that are not 16-byte vectors) and the
+    LSD sort passes (more than 2^22 padded keys)."""
+    b = w.ROUNDTRIP_BATCHING_INDEX
+    Y = b["A"] * b["BS"] * b["K1"]
+    assert Y > 32768 and b["H"] * 2 == 16 and Y * b["H"] * 2 // 16 >= 65536
+    m = w.UNPERMUTE_LARGE_MAP
+    assert m["T"] * m["Eu"] > (1 << 22)
+    o = w.UNPERMUTE_ODD_H
+    assert (o["H"] * w.ELEM_BYTES[o["dtype"]]) % 16 != 0
+    pl = w.UNPERMUTE_PADDED_LSD
+    assert pl["T"] + 1 > (1 << 22)
+    src = open(bench.__file__).read()
+    for name in ("batching_index", "large_map", "odd_h", "padded_lsd"):
+        assert f'"{name}"' in src
