@@ -10,7 +10,7 @@ namespace mr {
 // maskedSelect of probs.T by routingMap.T (not padded, with probs).
 // The routing map is cut into blocks of 32 tokens; item (blk, e) holds the
 // 32-bit mask of the block's tokens routed to expert e (built by one lane per
-// expert, reading 32 routing-map bytes). Its popcount is the
+// expert, or per four experts, reading 32 routing-map rows). Its popcount is the
 // histogram entry of the counting sort whose key is the expert, so the
 // engine's prefix kernel turns them into positions: the j-th token of the
 // mask lands at bucket_start[e] + tile_off[blk][e] + (set bits below j).
